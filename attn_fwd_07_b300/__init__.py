@@ -1,1 +1,205 @@
+"""attn_fwd_07_b300 -- exact FlashAttention-style attention for B300 (sm_103a).
 
+Python binding of ``libattn07.so`` (C ABI in ``include/attn07.h``).  The
+functions here have the C entry points' names and only marshal arguments:
+they read shapes from torch tensors, allocate outputs when none are given, and
+pass device pointers and the current CUDA stream to the library.  Every step of
+the computation runs in the library's CUDA kernels; there is no other path.
+If the library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = [
+    "AttnError", "load_library", "attn_fwd", "attn_fwd_f32", "attn_fwd_varlen",
+    "attn_decode_paged", "attn_decode_workspace_size", "attn_status_string",
+    "attn_get_device_status", "attn_version",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn07.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_DEVICE_BOUNDS = 5
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__("%s: %s (status %d)" % (where, attn_status_string(code), code))
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libattn07.so (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise OSError("libattn07.so not found at %s; build it with "
+                          "`python -m attn_fwd_07_b300.build`" % path)
+        lib = ctypes.CDLL(path)
+        P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]
+        lib.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.attn_decode_workspace_size.restype = SZ
+        lib.attn_status_string.argtypes = [I]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_get_device_status.argtypes = [P]
+        lib.attn_version.argtypes = []
+        lib.attn_version.restype = ctypes.c_char_p
+        for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
+                     "attn_get_device_status"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def attn_status_string(code: int) -> str:
+    return load_library().attn_status_string(int(code)).decode()
+
+
+def attn_version() -> str:
+    return load_library().attn_version().decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code, where):
+    if code != ATTN_OK:
+        raise AttnError(code, where)
+
+
+def _need(t, dtype, name):
+    if not (t.is_cuda and t.dtype == dtype and t.is_contiguous()):
+        raise ValueError("%s must be a contiguous CUDA %s tensor" % (name, dtype))
+
+
+def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, o=None, lse=None,
+             want_lse: bool = True, stream=None):
+    """bf16 prefill.  q [B,N,Hq,d], k/v [B,N,Hkv,d] -> (o [B,N,Hq,d] bf16, lse [B,Hq,N] fp32)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [B, N, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N,
+                                 d, int(bool(causal)), float(scale), _stream(stream))
+    _check(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_f32(q, k, v, causal: bool = True, scale: float | None = None, o=None, lse=None,
+                 want_lse: bool = True, stream=None):
+    """fp32 prefill, same layouts as attn_fwd."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.float32, n)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [B, N, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                     N, d, int(bool(causal)), float(scale), _stream(stream))
+    _check(rc, "attn_fwd_f32")
+    return o, lse
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = True,
+                    scale: float | None = None, o=None, lse=None, want_lse: bool = True,
+                    stream=None):
+    """Packed prefill.  q [T,Hq,d], k/v [T,Hkv,d], cu_seqlens int32 [S+1] on the device
+
+    -> (o [T,Hq,d] bf16, lse [Hq,T] fp32).
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [T, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                        _ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                        int(max_seqlen), Hq, Hkv, d, int(bool(causal)),
+                                        float(scale), _stream(stream))
+    _check(rc, "attn_fwd_varlen")
+    return o, lse
+
+
+def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, d: int, max_pages_per_seq: int,
+                               page_size: int) -> int:
+    return int(load_library().attn_decode_workspace_size(B, Hq, Hkv, d, max_pages_per_seq,
+                                                         page_size))
+
+
+def attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | None = None,
+                      o=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
+    """Decode against a paged cache.  q [B,Hq,d]; caches [P,page,Hkv,d]; page_table int32
+    [B,maxp]; seq_lens int32 [B] (device) -> (o [B,Hq,d] bf16, lse [B,Hq] fp32)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(page_table, torch.int32, "page_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, d = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    maxp = page_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = attn_decode_workspace_size(B, Hq, Hkv, d, maxp, ps)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = load_library().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
+                                          _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, ps, P,
+                                          maxp, float(scale), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    _check(rc, "attn_decode_paged")
+    return o, lse
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(load_library().attn_get_device_status(_stream(stream)))

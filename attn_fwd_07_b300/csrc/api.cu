@@ -1,0 +1,328 @@
+// api.cu -- the C ABI of libattn07.so (declared in include/attn07.h): argument
+// validation, tensor-map construction and kernel launches.  No entry point
+// allocates, frees or synchronises device memory (attn_get_device_status
+// synchronises its stream by design).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+#include <string.h>
+
+#include "attn07.h"
+#include "decode.cuh"
+#include "prefill_simt.cuh"
+#include "prefill_tc.cuh"
+
+using namespace attn07;
+
+// Device status word shared by every kernel of the library (per device).
+__device__ unsigned int g_attn_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    unsigned *status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+attn_status_t cuda_fail(cudaError_t e) {
+    (void)cudaGetLastError();
+    (void)e;
+    return ATTN_ERR_CUDA;
+}
+
+// Per-device one-time set-up: SM count, status word address, kernel attributes.
+attn_status_t device_state(DeviceState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        if ((e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        void *sym = nullptr;
+        if ((e = cudaGetSymbolAddress(&sym, g_attn_status)) != cudaSuccess) return cuda_fail(e);
+        st.status = static_cast<unsigned *>(sym);
+        if ((e = cudaFuncSetAttribute(prefill_simt_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)prefill_simt_smem_bytes(kSimtMaxD))) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaFuncSetAttribute(prefill_tc_kernel<128>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)PrefillCfg<128>::SMEM)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaFuncSetAttribute(prefill_tc_kernel<64>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)PrefillCfg<64>::SMEM)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaFuncSetAttribute(decode_split_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      227 * 1024)) != cudaSuccess)
+            return cuda_fail(e);
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void *fn = nullptr;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(e);
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        st.ready = true;
+    }
+    *out = &st;
+    return ATTN_OK;
+}
+
+// bf16 tensor map, 128-byte swizzle, box inner extent 64 elements.
+attn_status_t make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
+                       const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+                          const_cast<void *>(ptr), dims, strides_bytes, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch the tensor-core prefill on a [tokens, heads, d] layout with
+// `nbatch` sequences along the outermost axis (dense) or one packed axis (varlen).
+attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, void *o, float *lse,
+                                const int32_t *cu_seqlens, int nseq, int N_or_total,
+                                int ntiles, int Hq, int Hkv, int d, int causal, float scale,
+                                cudaStream_t stream) {
+    DeviceState *st = nullptr;
+    attn_status_t s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    const bool varlen = cu_seqlens != nullptr;
+    // dims innermost first: d, heads, tokens, batch
+    const cuuint64_t nb = varlen ? 1 : (cuuint64_t)nseq;
+    const cuuint64_t dq[4] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)N_or_total, nb};
+    const cuuint64_t dk[4] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)N_or_total, nb};
+    const cuuint64_t sq[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hq * d * 2,
+                              (cuuint64_t)N_or_total * Hq * d * 2};
+    const cuuint64_t sk[3] = {(cuuint64_t)d * 2, (cuuint64_t)Hkv * d * 2,
+                              (cuuint64_t)N_or_total * Hkv * d * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    CUtensorMap mq, mk, mv;
+    if ((s = make_map(&mq, q, 4, dq, sq, box)) != ATTN_OK) return s;
+    if ((s = make_map(&mk, k, 4, dk, sk, box)) != ATTN_OK) return s;
+    if ((s = make_map(&mv, v, 4, dk, sk, box)) != ATTN_OK) return s;
+    PrefillParams p;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.lse = lse;
+    p.cu_seqlens = cu_seqlens;
+    p.status = st->status;
+    p.N = varlen ? 0 : N_or_total;
+    p.nseq = nseq;
+    p.total = varlen ? N_or_total : 0;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.ntiles = ntiles;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    const long long grid = (long long)ntiles * Hq * nseq;
+    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (grid == 0) return ATTN_OK;
+    if (d == 128) {
+        prefill_tc_kernel<128><<<(unsigned)grid, 192, PrefillCfg<128>::SMEM, stream>>>(p, mq, mk, mv);
+    } else {
+        prefill_tc_kernel<64><<<(unsigned)grid, 192, PrefillCfg<64>::SMEM, stream>>>(p, mq, mk, mv);
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *attn_version(void) { return "attn07 0.1.0 sm_103a"; }
+
+const char *attn_status_string(attn_status_t s) {
+    switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported size or configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_DEVICE_BOUNDS: return "device found an index out of range";
+    }
+    return "unknown status";
+}
+
+attn_status_t attn_get_device_status(attn_stream_t stream) {
+    DeviceState *st = nullptr;
+    attn_status_t s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned v = 0;
+    e = cudaMemcpy(&v, st->status, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(st->status, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return (attn_status_t)v;
+}
+
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                       int Hq, int Hkv, int N, int d, int causal, float scale,
+                       attn_stream_t stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)B * N * Hq * d > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
+    const int ntiles = (N + 127) / 128;
+    return launch_prefill_tc(q, k, v, o, lse, nullptr, B, N, ntiles, Hq, Hkv, d, causal, scale,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                              int max_seqlen, int Hq, int Hkv, int d, int causal, float scale,
+                              attn_stream_t stream) {
+    if (!q || !k || !v || !o || !cu_seqlens) return ATTN_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || total_tokens < 0 || max_seqlen < 0 || Hq <= 0 || Hkv <= 0 ||
+        Hq % Hkv != 0 || d <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
+    const int ntiles = (max_seqlen + 127) / 128;
+    return launch_prefill_tc(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, ntiles, Hq, Hkv,
+                             d, causal, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+                           int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                           attn_stream_t stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (d > kSimtMaxD || d % 16 != 0) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+    DeviceState *st = nullptr;
+    attn_status_t s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    SimtParams p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.o = o;
+    p.lse = lse;
+    p.cu_seqlens = nullptr;
+    p.N = N;
+    p.total = 0;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * kLog2e;
+    dim3 grid((N + kSimtBM - 1) / kSimtBM, Hq, B);
+    prefill_simt_kernel<<<grid, kSimtThreads, prefill_simt_smem_bytes(d),
+                          reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_per_seq,
+                                  int page_size) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || max_pages_per_seq <= 0 || page_size <= 0)
+        return 0;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != ATTN_OK) return 0;
+    const size_t slots = (size_t)B + (size_t)st->sms;
+    const size_t bytes_o = slots * Hq * d * sizeof(float);
+    const size_t bytes_l = slots * Hq * sizeof(float);
+    return ((bytes_o + 255) & ~(size_t)255) + bytes_l;
+}
+
+attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *page_table, const int32_t *seq_lens, void *o,
+                                float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                                int num_pages, int max_pages_per_seq, float scale,
+                                void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o || !workspace)
+        return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 ||
+        num_pages <= 0 || max_pages_per_seq <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+        !aligned16(workspace))
+        return ATTN_ERR_INVALID_ARG;
+    if (page_size != kDecPage || (d != 64 && d != 128) || Hkv > kDecMaxHkv || Hq / Hkv > 8)
+        return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, d, max_pages_per_seq, page_size);
+    if (need == 0) return ATTN_ERR_CUDA;
+    if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    attn_status_t s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    const size_t stage = dec_stage_bytes(Hkv, d);
+    int stages = (int)((220 * 1024 - 2048) / stage);
+    if (stages > kDecMaxStages) stages = kDecMaxStages;
+    if (stages < 2) return ATTN_ERR_UNSUPPORTED;
+    // cache as a 4-D tensor: (dim, token-in-page, head, page) so that one box
+    // lands in shared memory as [head][token][64 dims]
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)Hkv,
+                                (cuuint64_t)num_pages};
+    const cuuint64_t strides[3] = {(cuuint64_t)Hkv * d * 2, (cuuint64_t)d * 2,
+                                   (cuuint64_t)page_size * Hkv * d * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)page_size, (cuuint32_t)Hkv, 1};
+    CUtensorMap mk, mv;
+    if ((s = make_map(&mk, k_cache, 4, dims, strides, box)) != ATTN_OK) return s;
+    if ((s = make_map(&mv, v_cache, 4, dims, strides, box)) != ATTN_OK) return s;
+
+    const size_t slots = (size_t)B + (size_t)st->sms;
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                           ((slots * Hq * d * sizeof(float) + 255) & ~(size_t)255));
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.lse = lse;
+    p.status = st->status;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.num_pages = num_pages;
+    p.maxp = max_pages_per_seq;
+    p.stages = stages;
+    p.scale_log2 = scale * kLog2e;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const int G = st->sms;
+    const size_t smem = dec_smem_bytes(Hkv, d, stages);
+    decode_split_kernel<<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    decode_merge_kernel<<<B, 256, 0, cs>>>(p, G);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

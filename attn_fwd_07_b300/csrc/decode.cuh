@@ -1,0 +1,446 @@
+// decode.cuh -- decode attention against a paged key/value cache.
+//
+// What it computes: for every sequence b, one new query per query head
+// attends to all seq_lens[b] cached keys/values of its key/value head
+// (yapayzekasozluk.tr "attention" tag page, entry "KV Cache": cached keys and
+// values, grouped query heads sharing a key/value head, the cache held in
+// fixed-size pages).
+//
+// How (two kernels):
+//   decode_split_kernel  The cache pages of all sequences, taken in order
+//       (sequence 0's pages, then sequence 1's, ...), are cut into gridDim.x
+//       equal contiguous ranges, one per CTA, so every CTA streams the same
+//       number of pages whatever the length mix.  Within its range a CTA walks
+//       one or more "segments" (the part of one sequence inside the range) and
+//       keeps the online-softmax state ("Donanıma Duyarlı Algoritma Tasarımı:
+//       FlashAttention", section "Online Softmax Prensibi": running maximum,
+//       running sum, output rescaled when the maximum grows) per query head.
+//       At the end of a segment it writes the normalised partial output and
+//       its log-sum-exp to workspace slot (b + CTA index); along the
+//       monotone staircase of (sequence, CTA) pairs that touch, b + c is
+//       strictly increasing, so slots never collide and B + gridDim.x slots
+//       suffice.
+//   decode_merge_kernel  For each sequence, combines its partials by their
+//       log-sum-exps: lse = ln sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s
+//       (the same rescaling rule, applied across key ranges), writing bf16 O
+//       and fp32 LSE.
+//
+// Data movement: a TMA producer warp copies each page -- all key/value heads,
+// 16 tokens -- into a multi-stage shared-memory ring, as 128-byte-swizzled
+// boxes of [head][token][64 dims] so that each head's 16 token rows are
+// conflict-free for ldmatrix.  One consumer warp per key/value head computes
+// S = q K^T and O += P V for its Hq/Hkv query heads with mma.sync m16n8k16
+// (bf16 in, fp32 accumulate; the query heads fill the first rows of the
+// 16-row tile).  The decode is bound by device-memory bandwidth: the
+// contraction per byte is small, and the ring keeps enough bytes in flight.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace attn07 {
+
+constexpr int kDecPage = 16;          // tokens per page (the kernel is built for it)
+constexpr int kDecMaxStages = 4;
+constexpr int kDecMaxHkv = 8;
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;    // [B, Hq, d]
+    const int32_t *page_table; // [B, maxp]
+    const int32_t *seq_lens;   // [B]
+    float *part_o;             // [B + G, Hq, d]
+    float *part_lse;           // [B + G, Hq]
+    __nv_bfloat16 *o;          // [B, Hq, d]
+    float *lse;                // [B, Hq] or null
+    unsigned *status;
+    int B, Hq, Hkv, d, num_pages, maxp;
+    int stages;
+    float scale_log2;
+};
+
+struct DecodeStageMeta {
+    int b;        // sequence
+    int ntok;     // valid tokens in this page (0 if the page id was bad)
+    int first;    // first page of a segment
+    int last;     // last page of a segment
+};
+
+// Shared-memory layout (offsets from a 1024-byte-aligned base):
+//   stage s:  K half 0 .. K half (d/64 - 1), V half 0 .. V half (d/64 - 1),
+//             each [Hkv][16][64] bf16 = Hkv * 2048 bytes
+//   then full[kDecMaxStages], empty[kDecMaxStages] mbarriers, meta, scalars.
+__host__ __device__ inline uint32_t dec_half_bytes(int Hkv) { return (uint32_t)Hkv * 16u * 128u; }
+__host__ __device__ inline uint32_t dec_stage_bytes(int Hkv, int d) {
+    return 2u * (uint32_t)(d / 64) * dec_half_bytes(Hkv);
+}
+__host__ __device__ inline uint32_t dec_ctrl_bytes() { return 1024u; }
+inline size_t dec_smem_bytes(int Hkv, int d, int stages) {
+    return 1024 /* alignment slack */ + (size_t)stages * dec_stage_bytes(Hkv, d) + dec_ctrl_bytes();
+}
+
+// ceil(len / 16) pages of sequence b
+__device__ __forceinline__ int dec_pages_of(const int32_t *seq_lens, int b) {
+    const int len = seq_lens[b];
+    return len > 0 ? (len + kDecPage - 1) / kDecPage : 0;
+}
+
+// The CTA whose page range [c*T/G, (c+1)*T/G) holds global page x.
+__host__ __device__ __forceinline__ int dec_cta_of_page(long long x, long long T, long long G) {
+    return (int)(((x + 1) * G - 1) / T);
+}
+
+// Whether CTA c's page range is non-empty.  Every CTA strictly between the ones
+// holding a sequence's first and last page lies inside that sequence, so for
+// those CTAs "non-empty" is the same as "wrote a partial for it".
+__host__ __device__ __forceinline__ bool dec_range_nonempty(long long c, long long T, long long G) {
+    return (c + 1) * T / G > c * T / G;
+}
+
+__global__ void __launch_bounds__(32 * (kDecMaxHkv + 1), 1)
+decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV) {
+    extern __shared__ uint8_t dec_smem_raw[];
+    const uint32_t raw = smem_u32(dec_smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = dec_smem_raw + (base - raw);
+
+    const int S = p.stages;
+    const uint32_t stage_bytes = dec_stage_bytes(p.Hkv, p.d);
+    const uint32_t half_bytes = dec_half_bytes(p.Hkv);
+    const int nhalf = p.d / 64;
+    const uint32_t ctrl = base + (uint32_t)S * stage_bytes;
+    uint8_t *ctrl_ptr = base_ptr + (size_t)S * stage_bytes;
+    // control block: full[4] @0, empty[4] @32, meta[4] @64, scalars @192
+    const uint32_t full0 = ctrl, empty0 = ctrl + 32;
+    DecodeStageMeta *meta = reinterpret_cast<DecodeStageMeta *>(ctrl_ptr + 64);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl_ptr + 192);
+    int *shared_n = reinterpret_cast<int *>(ctrl_ptr + 196);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int Hkv = p.Hkv;
+    const int G = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, Hkv);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+
+    // ---- this CTA's page range (computed by the producer warp, published)
+    long long T = 0;  // total pages of all sequences
+    if (warp == Hkv) {
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+            int np = (b0 + lane < p.B) ? dec_pages_of(p.seq_lens, b0 + lane) : 0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) np += __shfl_xor_sync(0xffffffffu, np, o);
+            T += np;
+        }
+        if (lane == 0) {
+            const long long p0 = (long long)blockIdx.x * T / G;
+            const long long p1 = (long long)(blockIdx.x + 1) * T / G;
+            *shared_n = (int)(p1 - p0);
+        }
+    }
+    __syncthreads();
+    const int n_iter = *shared_n;
+
+    if (warp == Hkv) {
+        // ================= producer: page ids -> TMA into the ring
+        const long long p0 = (long long)blockIdx.x * T / G;
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+        }
+        const uint64_t pol = policy_evict_first();
+        // find the sequence holding global page p0
+        int b = 0;
+        long long seq_start = 0;  // global index of sequence b's first page
+        int np_b = 0;
+        if (n_iter > 0) {
+            for (;;) {
+                np_b = dec_pages_of(p.seq_lens, b);
+                if (seq_start + np_b > p0) break;
+                seq_start += np_b;
+                ++b;
+            }
+        }
+        int lp = (int)(p0 - seq_start);   // logical page within sequence b
+        int ids_base = -1;                // logical page of ids[lane] batch start
+        int my_id = 0;
+        const uint32_t tx = stage_bytes;
+        for (int it = 0; it < n_iter; ++it) {
+            // advance to the next non-empty sequence when the current one is done
+            while (lp >= np_b) {
+                ++b;
+                lp = 0;
+                np_b = dec_pages_of(p.seq_lens, b);
+                ids_base = -1;
+            }
+            if (ids_base < 0 || lp >= ids_base + 32) {
+                ids_base = lp;
+                my_id = (lp + lane < np_b) ? p.page_table[(long long)b * p.maxp + lp + lane] : 0;
+            }
+            const int pid = __shfl_sync(0xffffffffu, my_id, lp - ids_base);
+            const int s = it % S;
+            const uint32_t par = ((uint32_t)(it / S) & 1u) ^ 1u;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(empty0 + 8 * s, par, p.status, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            const bool last_of_seq = (lp == np_b - 1);
+            if (lane == 0) {
+                const bool valid = (unsigned)pid < (unsigned)p.num_pages;
+                DecodeStageMeta mt;
+                mt.b = b;
+                mt.ntok = valid ? (last_of_seq ? p.seq_lens[b] - lp * kDecPage : kDecPage) : 0;
+                mt.first = (it == 0 || lp == 0) ? 1 : 0;
+                mt.last = (it == n_iter - 1 || last_of_seq) ? 1 : 0;
+                meta[s] = mt;
+                const uint32_t dst = base + (uint32_t)s * stage_bytes;
+                if (valid) {
+                    mbar_arrive_expect_tx(full0 + 8 * s, tx);
+                    for (int hf = 0; hf < nhalf; ++hf) {
+                        tma_load_4d(dst + hf * half_bytes, &tmK, full0 + 8 * s, hf * 64, 0, 0,
+                                    pid, pol);
+                        tma_load_4d(dst + (nhalf + hf) * half_bytes, &tmV, full0 + 8 * s,
+                                    hf * 64, 0, 0, pid, pol);
+                    }
+                } else {
+                    record_status(p.status, kStatusBounds);
+                    mbar_arrive(full0 + 8 * s);
+                }
+            }
+            ++lp;
+        }
+    } else if (warp < Hkv) {
+        // ================= consumers: warp g serves kv head g
+        const int g = warp;
+        const int Gq = p.Hq / Hkv;             // query heads per kv head (<= 8)
+        const int row = lane >> 2;             // mma row = query head within group
+        const int quad = lane & 3;
+        const bool row_ok = row < Gq;
+        const int nk = p.d / 16;               // k-steps of S = q K^T
+        const int nd = p.d / 8;                // n-tiles of O
+
+        uint32_t qa[8][2];                     // A fragments of q (rows 0..7)
+        float oacc[16][4];
+        float m_run = -INFINITY, l_run = 0.f, q_run = 0.f;
+        int cur_b = 0;
+
+        for (int it = 0; it < n_iter; ++it) {
+            const int s = it % S;
+            const uint32_t par = (uint32_t)(it / S) & 1u;
+            bool ok = mbar_wait(full0 + 8 * s, par, p.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const DecodeStageMeta mt = meta[s];
+            if (mt.first) {
+                cur_b = mt.b;
+                const __nv_bfloat16 *qb = p.q + ((long long)cur_b * p.Hq + g * Gq) * p.d;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    if (ks < nk && row_ok) {
+                        const uint32_t *qr = reinterpret_cast<const uint32_t *>(qb + row * p.d);
+                        qa[ks][0] = qr[(ks * 16 + 2 * quad) >> 1];
+                        qa[ks][1] = qr[(ks * 16 + 8 + 2 * quad) >> 1];
+                    } else {
+                        qa[ks][0] = 0u;
+                        qa[ks][1] = 0u;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+                m_run = -INFINITY;
+                l_run = 0.f;
+                q_run = 0.f;
+            }
+            const uint32_t kst = base + (uint32_t)s * stage_bytes;
+            const uint32_t vst = kst + (uint32_t)nhalf * half_bytes;
+            if (mt.ntok > 0) {
+                // ---- S = q K^T over the 16 tokens (two n-tiles of 8 tokens)
+                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                {
+                    const int mi = lane >> 3, i = lane & 7;
+                    const int tok = (mi >> 1) * 8 + i;
+                    const uint32_t r = (uint32_t)(g * 16 + tok);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        if (ks < nk) {
+                            const int hf = ks >> 2;
+                            const int chunk = (ks & 3) * 2 + (mi & 1);
+                            const uint32_t addr = kst + hf * half_bytes + r * 128u +
+                                                  (uint32_t)((chunk ^ (int)(r & 7u)) * 16);
+                            uint32_t b00, b01, b10, b11;
+                            ldsm_x4(addr, b00, b01, b10, b11);
+                            mma_bf16_16816(sacc[0], qa[ks][0], 0u, qa[ks][1], 0u, b00, b01);
+                            mma_bf16_16816(sacc[1], qa[ks][0], 0u, qa[ks][1], 0u, b10, b11);
+                        }
+                    }
+                }
+                // ---- mask, online softmax (rows = query heads, 4 lanes per row)
+                float sv[4];
+                sv[0] = sacc[0][0] * p.scale_log2;
+                sv[1] = sacc[0][1] * p.scale_log2;
+                sv[2] = sacc[1][0] * p.scale_log2;
+                sv[3] = sacc[1][1] * p.scale_log2;
+                const int t0 = 2 * quad;
+                if (t0 >= mt.ntok) sv[0] = -INFINITY;
+                if (t0 + 1 >= mt.ntok) sv[1] = -INFINITY;
+                if (t0 + 8 >= mt.ntok) sv[2] = -INFINITY;
+                if (t0 + 9 >= mt.ntok) sv[3] = -INFINITY;
+                float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(m_run, mx);
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                const float alpha = ex2(m_run - m_use);
+                float pr[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) pr[j] = ex2(sv[j] - m_use);
+                // P enters the PV product as bf16; O is normalised by the sum of the same
+                // rounded values, the log-sum-exp by the exact sum
+                const uint32_t pa0 = pack_bf16(pr[0], pr[1]);
+                const uint32_t pa2 = pack_bf16(pr[2], pr[3]);
+                float pq = (bf16lo(pa0) + bf16hi(pa0)) + (bf16lo(pa2) + bf16hi(pa2));
+                float ps = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+                pq += __shfl_xor_sync(0xffffffffu, pq, 1);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+                pq += __shfl_xor_sync(0xffffffffu, pq, 2);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+                l_run = l_run * alpha + ps;   // exact sum -> log-sum-exp
+                q_run = q_run * alpha + pq;   // sum of the rounded P -> normalises O
+                m_run = m_new;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    oacc[j][0] *= alpha;
+                    oacc[j][1] *= alpha;
+                }
+                // ---- O += P V
+                {
+                    const int mi = lane >> 3, i = lane & 7;
+                    const int tok = (mi & 1) * 8 + i;
+                    const uint32_t r = (uint32_t)(g * 16 + tok);
+#pragma unroll
+                    for (int dn = 0; dn < 16; dn += 2) {
+                        if (dn < nd) {
+                            const int hf = dn >> 3;
+                            const int chunk = (dn & 7) + (mi >> 1);
+                            const uint32_t addr = vst + hf * half_bytes + r * 128u +
+                                                  (uint32_t)((chunk ^ (int)(r & 7u)) * 16);
+                            uint32_t v0, v1, v2, v3;
+                            ldsm_x4_t(addr, v0, v1, v2, v3);
+                            mma_bf16_16816(oacc[dn], pa0, 0u, pa2, 0u, v0, v1);
+                            mma_bf16_16816(oacc[dn + 1], pa0, 0u, pa2, 0u, v2, v3);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (mt.last) {
+                // ---- partial result of this segment -> workspace slot b + cta
+                const long long slot = (long long)cur_b + blockIdx.x;
+                if (row_ok) {
+                    const int h = g * Gq + row;
+                    const float inv = (q_run > 0.f) ? 1.f / q_run : 0.f;
+                    float *po = p.part_o + (slot * p.Hq + h) * p.d;
+#pragma unroll
+                    for (int dn = 0; dn < 16; ++dn) {
+                        if (dn < nd) {
+                            *reinterpret_cast<float2 *>(po + dn * 8 + 2 * quad) =
+                                make_float2(oacc[dn][0] * inv, oacc[dn][1] * inv);
+                        }
+                    }
+                    if (quad == 0) {
+                        p.part_lse[slot * p.Hq + h] =
+                            (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+                    }
+                }
+            }
+        }
+    }
+    __syncwarp();
+    __syncthreads();
+}
+
+// One CTA per sequence: combine the partial results of the CTAs that covered it.
+__global__ void __launch_bounds__(256)
+decode_merge_kernel(const DecodeParams p, int G) {
+    __shared__ long long red[2][8];
+    const int b = blockIdx.x;
+    // start page of sequence b and total pages T
+    long long before = 0, total = 0;
+    for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+        const int np = dec_pages_of(p.seq_lens, i);
+        total += np;
+        if (i < b) before += np;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        total += __shfl_xor_sync(0xffffffffu, total, o);
+    }
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        red[0][warp] = before;
+        red[1][warp] = total;
+    }
+    __syncthreads();
+    before = 0;
+    total = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        before += red[0][w];
+        total += red[1][w];
+    }
+    const int np = dec_pages_of(p.seq_lens, b);
+    const int dq = p.d / 4;
+    if (np == 0) {
+        for (int idx = threadIdx.x; idx < p.Hq * dq; idx += blockDim.x) {
+            const int h = idx / dq, c = (idx % dq) * 4;
+            __nv_bfloat16 *ob = p.o + ((long long)b * p.Hq + h) * p.d + c;
+            *reinterpret_cast<uint2 *>(ob) = make_uint2(0u, 0u);
+            if (p.lse && c == 0) p.lse[(long long)b * p.Hq + h] = -INFINITY;
+        }
+        return;
+    }
+    const int c0 = dec_cta_of_page(before, total, G);
+    const int c1 = dec_cta_of_page(before + np - 1, total, G);
+    for (int idx = threadIdx.x; idx < p.Hq * dq; idx += blockDim.x) {
+        const int h = idx / dq, c = (idx % dq) * 4;
+        // CTAs c0..c1 cover the sequence's pages; a CTA whose range is empty (more CTAs
+        // than pages) wrote nothing and is skipped
+        float mx = -INFINITY;
+        for (int cc = c0; cc <= c1; ++cc)
+            if (dec_range_nonempty(cc, total, G))
+                mx = fmaxf(mx, p.part_lse[((long long)b + cc) * p.Hq + h]);
+        float wsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (mx != -INFINITY) {
+            for (int cc = c0; cc <= c1; ++cc) {
+                if (!dec_range_nonempty(cc, total, G)) continue;
+                const long long slot = (long long)b + cc;
+                const float ls = p.part_lse[slot * p.Hq + h];
+                const float w = ex2((ls - mx) * kLog2e);
+                wsum += w;
+                const float4 po =
+                    *reinterpret_cast<const float4 *>(p.part_o + (slot * p.Hq + h) * p.d + c);
+                acc.x = fmaf(w, po.x, acc.x);
+                acc.y = fmaf(w, po.y, acc.y);
+                acc.z = fmaf(w, po.z, acc.z);
+                acc.w = fmaf(w, po.w, acc.w);
+            }
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        __nv_bfloat16 *ob = p.o + ((long long)b * p.Hq + h) * p.d + c;
+        *reinterpret_cast<uint2 *>(ob) =
+            make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+        if (p.lse && c == 0)
+            p.lse[(long long)b * p.Hq + h] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
+    }
+}
+
+}  // namespace attn07

@@ -1,0 +1,171 @@
+/*
+ * attn07.h -- C ABI of the B300 (sm_103a) exact-attention library libattn07.so.
+ *
+ * Operation.  Exact scaled-dot-product attention, O = softmax(Q K^T * scale) V,
+ * as stated in "Donanıma Duyarlı Algoritma Tasarımı: FlashAttention"
+ * (fatihsoysal.com), section "Transformer Mimarisi ve Self-Attention
+ * Mekanizması" (the attention formula; Q, K, V are (sequence, dimension)
+ * matrices; the softmax is taken over each row of Q K^T).  The result is the
+ * exact one, not an approximation (yapayzekasozluk.tr "attention" tag page,
+ * entry "Flash Attention"), computed tile by tile on chip with the online
+ * softmax of the same fatihsoysal.com page, section "Online Softmax
+ * Prensibi", so that the N x N score matrix never reaches device memory.
+ *
+ * For query head h the key/value head is h / (Hq / Hkv): groups of Hq/Hkv
+ * consecutive query heads share one key/value head (grouped-query attention,
+ * yapayzekasozluk.tr "attention" tag page, entry "KV Cache").
+ *
+ * Log-sum-exp output.  Where an `lse` pointer is accepted, row r receives
+ * LSE_r = ln sum_j exp(s_rj) over the row's allowed keys, s_rj = scale * q_r . k_j
+ * (natural log, of the scaled scores), in fp32.  A row with no allowed key gets
+ * O = 0 and LSE = -inf.  `lse` may be NULL when it is not wanted.
+ *
+ * Causal masking.  With causal != 0, query i of a sequence sees keys j <= i
+ * (queries and keys of a sequence share positions).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller; the
+ *     library allocates, frees and synchronises nothing (the single exception
+ *     is attn_get_device_status, which synchronises `stream` by design).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and runs asynchronously; the return value reports argument
+ *     validation and launch errors only.
+ *   - Invalid arguments return ATTN_ERR_INVALID_ARG and launch nothing;
+ *     sizes outside what the kernels implement return ATTN_ERR_UNSUPPORTED and
+ *     launch nothing.  Launch failures return ATTN_ERR_CUDA.
+ *   - Errors found on the device (a page id out of range; a pipeline wait that
+ *     ran past its bound) never fault the device: the kernel records them in a
+ *     device status word, skips the access, and
+ *     attn_get_device_status() reports them.
+ *   - Entry points are thread-safe and re-entrant.
+ *   - bf16 means IEEE bfloat16 (1-8-7) stored in 2 bytes, round-to-nearest-even
+ *     on output.
+ */
+#ifndef ATTN07_H
+#define ATTN07_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, page size, ...) */
+    ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+    ATTN_ERR_TIMEOUT = 4,      /* a device-side pipeline wait ran past its bound */
+    ATTN_ERR_DEVICE_BOUNDS = 5 /* the device found an index out of range (page id) */
+} attn_status_t;
+
+/*
+ * attn_fwd -- batched prefill attention, bf16 in, bf16 out.
+ * Source: the attention formula (fatihsoysal.com page, section "Transformer
+ * Mimarisi ve Self-Attention Mekanizması") computed with the tiling and online
+ * softmax of sections "FlashAttention'ın Temelleri" and "Online Softmax
+ * Prensibi", work split over query-row tiles as in section
+ * "FlashAttention-2: Optimizasyonlar ve İyileştirmeler".
+ *   q   [B, N, Hq,  d] bf16, contiguous (token-major, then head, then dim)
+ *   k,v [B, N, Hkv, d] bf16, contiguous
+ *   o   [B, N, Hq,  d] bf16, written
+ *   lse [B, Hq, N]     fp32, written, or NULL
+ *   B >= 1, N >= 1, Hq >= 1, Hkv >= 1, Hq % Hkv == 0.
+ *   d must be 64 or 128 (else ATTN_ERR_UNSUPPORTED).  scale is typically
+ *   1/sqrt(d).  Pointers must be 16-byte aligned.
+ */
+attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                       attn_stream_t stream);
+
+/*
+ * attn_fwd_f32 -- the same operation with fp32 q, k, v and o (same layouts and
+ * rules as attn_fwd).  Arithmetic is fp32 throughout (no reduced-precision
+ * tensor-core path).  1 <= d <= 128 and d % 4 == 0.
+ */
+attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float *o,
+                           float *lse, int B, int Hq, int Hkv, int N, int d, int causal,
+                           float scale, attn_stream_t stream);
+
+/*
+ * attn_fwd_varlen -- prefill over sequences of different lengths packed along
+ * the token axis; each sequence is an independent attention problem.
+ *   q   [total_tokens, Hq,  d] bf16      k,v [total_tokens, Hkv, d] bf16
+ *   o   [total_tokens, Hq,  d] bf16      lse [Hq, total_tokens] fp32 or NULL
+ *   cu_seqlens  int32 [num_seqs + 1], DEVICE pointer: sequence s owns tokens
+ *               cu_seqlens[s] .. cu_seqlens[s+1]-1; cu_seqlens[0] = 0,
+ *               non-decreasing, cu_seqlens[num_seqs] = total_tokens.
+ *   max_seqlen  host-side upper bound on every sequence length (sizes the
+ *               launch; a sequence longer than it is not fully computed).
+ *   Zero-length sequences are allowed.  d must be 64 or 128.
+ */
+attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                              int max_seqlen, int Hq, int Hkv, int d, int causal, float scale,
+                              attn_stream_t stream);
+
+/*
+ * attn_decode_paged -- one new query token per sequence attending to that
+ * sequence's cached keys and values held in fixed-size pages
+ * (yapayzekasozluk.tr "attention" tag page, entry "KV Cache": cached keys and
+ * values, grouped query heads, a cache kept in fixed-size pages).  The query
+ * sees every cached token (no mask).  The key range of each sequence is split
+ * over the GPU, each piece is attended with the online softmax, and the pieces
+ * are combined by their log-sum-exps (the rescaling rule of section "Online
+ * Softmax Prensibi" of the fatihsoysal.com page).
+ *   q           [B, Hq, d] bf16
+ *   k_cache,
+ *   v_cache     [num_pages, page_size, Hkv, d] bf16
+ *   page_table  int32 [B, max_pages_per_seq]: entry p of sequence b is the
+ *               physical page holding its tokens p*page_size .. p*page_size+page_size-1;
+ *               only the first ceil(seq_lens[b]/page_size) entries are read.
+ *   seq_lens    int32 [B]: cached tokens per sequence, 0 <= seq_lens[b] <=
+ *               max_pages_per_seq * page_size.  DEVICE pointer (read on the device).
+ *   o           [B, Hq, d] bf16, written;  lse [B, Hq] fp32 or NULL.
+ *   workspace   device scratch of at least attn_decode_workspace_size(...) bytes,
+ *               16-byte aligned, owned by the caller; its contents on entry do
+ *               not matter and are overwritten.
+ *   Supported: page_size == 16, d in {64, 128}, Hq/Hkv <= 8, Hkv <= 16 (and one
+ *   page of keys plus values for all heads must fit three times in shared memory).
+ *   A page id outside [0, num_pages) is not read: its tokens are treated as
+ *   masked and ATTN_ERR_DEVICE_BOUNDS is recorded for attn_get_device_status.
+ *   A sequence with seq_lens[b] == 0 gets O = 0, LSE = -inf.
+ */
+attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *page_table, const int32_t *seq_lens, void *o,
+                                float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                                int num_pages, int max_pages_per_seq, float scale,
+                                void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Bytes of workspace attn_decode_paged needs for these sizes (0 on invalid
+ * sizes).  It depends only on B, Hq, d and the GPU's SM count, never on the
+ * sequence lengths.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_per_seq,
+                                  int page_size);
+
+/* Static, human-readable text for a status code. */
+const char *attn_status_string(attn_status_t s);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word shared
+ * by all kernels of this library on the current device.  Returns ATTN_OK if no
+ * kernel recorded an error since the last call, else the first recorded error
+ * (ATTN_ERR_TIMEOUT or ATTN_ERR_DEVICE_BOUNDS), or ATTN_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+attn_status_t attn_get_device_status(attn_stream_t stream);
+
+/* Library version, e.g. "attn07 0.1.0 sm_103a". */
+const char *attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN07_H */

@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library loads, exports every function the header
+declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attn_fwd_07_b300 as A
+from attn_fwd_07_b300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn07.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return A.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
+                 "attn_decode_workspace_size", "attn_status_string", "attn_get_device_status"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = A.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert A.attn_status_string(99) == "unknown status"
+    assert "sm_103a" in A.attn_version()
+
+
+def _fwd(lib, q=1 << 20, k=1 << 20, v=1 << 20, o=1 << 20, B=1, Hq=1, Hkv=1, N=8, d=128,
+         causal=1, scale=0.1):
+    P = ctypes.c_void_p
+    return lib.attn_fwd(P(q) if q else None, P(k) if k else None, P(v) if v else None,
+                        P(o) if o else None, None, B, Hq, Hkv, N, d, causal, scale, None)
+
+
+def test_fwd_argument_validation(lib):
+    # null pointers, bad sizes, head grouping, scale, alignment: rejected on the host
+    assert _fwd(lib, q=0) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, o=0) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, N=0) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, Hq=3, Hkv=2) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == A.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, q=(1 << 20) + 2) == A.ATTN_ERR_INVALID_ARG
+    # valid but not implemented head dims
+    assert _fwd(lib, d=96) == A.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, d=256) == A.ATTN_ERR_UNSUPPORTED
+
+
+def test_varlen_and_decode_validation(lib):
+    P = ctypes.c_void_p
+    p = P(1 << 20)
+    assert lib.attn_fwd_varlen(p, p, p, p, None, None, 2, 10, 8, 1, 1, 128, 1, 0.1,
+                               None) == A.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_varlen(p, p, p, p, None, p, 2, 10, 8, 4, 3, 128, 1, 0.1,
+                               None) == A.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_varlen(p, p, p, p, None, p, 2, 10, 8, 4, 2, 80, 1, 0.1,
+                               None) == A.ATTN_ERR_UNSUPPORTED
+    # decode: missing workspace, bad page size, too many query heads per kv head
+    args = [p, p, p, p, p, p, None, 4, 32, 8, 128, 16, 100, 10, 0.1]
+    assert lib.attn_decode_paged(*args, None, 0, None) == A.ATTN_ERR_INVALID_ARG
+    bad_ps = list(args)
+    bad_ps[11] = 32
+    assert lib.attn_decode_paged(*bad_ps, p, 1 << 30, None) == A.ATTN_ERR_UNSUPPORTED
+    bad_g = list(args)
+    bad_g[8], bad_g[9] = 64, 4
+    assert lib.attn_decode_paged(*bad_g, p, 1 << 30, None) == A.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_decode_workspace_size(0, 32, 8, 128, 10, 16) == 0
+
+
+def test_binding_requires_library(tmp_path):
+    """The binding raises rather than falling back when the library is absent."""
+    import importlib
+    mod = importlib.reload(A)
+    try:
+        with pytest.raises(OSError):
+            mod.load_library(str(tmp_path / "missing.so"))
+    finally:
+        importlib.reload(A)

@@ -1,0 +1,60 @@
+"""The benchmark's multi-process logic on CPU: two gloo ranks aggregate their
+timings the way bench.py does under torchrun (max of times, sum of work), and
+the reference arm's non-zero ranks do no work."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    w, r = bench.dist_init("gloo")
+    assert (w, r) == (world, rank)
+    t_max = bench.max_over_ranks(10.0 + rank, w)
+    work = bench.sum_over_ranks(100.0 * (rank + 1), w)
+    bench.barrier(w)
+    out[rank] = (t_max, work)
+    torch.distributed.destroy_process_group()
+
+
+def test_two_rank_aggregation_gloo():
+    world = 2
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn",
+                       join=True)
+    for r in range(world):
+        assert out[r] == (11.0, 300.0)
+
+
+def test_single_process_aggregation_is_identity():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.sum_over_ranks(2.0, 1) == 2.0
+
+
+def test_reference_arm_nonzero_rank_does_nothing(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert rc == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
