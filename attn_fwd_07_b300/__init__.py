@@ -17,7 +17,8 @@ import torch
 
 __all__ = [
     "AttnError", "load_library", "attn_fwd", "attn_fwd_f32", "attn_fwd_varlen",
-    "attn_decode_paged", "attn_decode_workspace_size", "attn_status_string",
+    "attn_decode_paged", "attn_decode_paged_noalloc", "attn_decode_workspace_size",
+    "attn_status_string",
     "attn_get_device_status", "attn_version",
 ]
 
@@ -53,6 +54,8 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]
+        lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
+                                                  P]
         lib.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I]
         lib.attn_decode_workspace_size.restype = SZ
         lib.attn_status_string.argtypes = [I]
@@ -61,7 +64,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_version.argtypes = []
         lib.attn_version.restype = ctypes.c_char_p
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
-                     "attn_get_device_status"):
+                     "attn_decode_paged_noalloc", "attn_get_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -197,6 +200,33 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | 
                                           workspace.numel() * workspace.element_size(),
                                           _stream(stream))
     _check(rc, "attn_decode_paged")
+    return o, lse
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, page_table, seq_lens,
+                              scale: float | None = None, o=None, lse=None,
+                              want_lse: bool = True, stream=None):
+    """attn_decode_paged without a workspace, for callers that cannot allocate device
+    memory (the library's built-in scratch array is used instead; calls that overlap
+    on the GPU race on it).  Same arguments and results as attn_decode_paged."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(page_table, torch.int32, "page_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, d = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    maxp = page_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_decode_paged_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                  _ptr(page_table), _ptr(seq_lens), _ptr(o),
+                                                  _ptr(lse), B, Hq, Hkv, d, ps, P, maxp,
+                                                  float(scale), _stream(stream))
+    _check(rc, "attn_decode_paged_noalloc")
     return o, lse
 
 

@@ -325,4 +325,46 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- no-allocation decode
+// Scratch for attn_decode_paged_noalloc: a fixed device array that every GPU
+// loading this library holds until exit.  Host code only ever sees a host-side
+// stand-in for its name; the device address is looked up per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+}  // namespace
+
+attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                        const int32_t *page_table, const int32_t *seq_lens,
+                                        void *o, float *lse, int B, int Hq, int Hkv, int d,
+                                        int page_size, int num_pages, int max_pages_per_seq,
+                                        float scale, attn_stream_t stream) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, d, max_pages_per_seq, page_size);
+    if (need == 0) return ATTN_ERR_CUDA;
+    if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            // once per device, with that device current
+            void *ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess || !ptr) return cuda_fail(e);
+            g_noalloc_ptr[dev] = ptr;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
+                             page_size, num_pages, max_pages_per_seq, scale, scratch,
+                             (size_t)ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 }  // extern "C"

@@ -161,6 +161,33 @@ const char *attn_status_string(attn_status_t s);
  */
 attn_status_t attn_get_device_status(attn_stream_t stream);
 
+/*
+ * attn_decode_paged_noalloc -- attn_decode_paged for callers that cannot
+ * allocate device memory: a host that hands the library only its input and
+ * output buffers (a plugin interface with no workspace to lend), or a serving
+ * process that reserved all device memory up front and may not call cudaMalloc
+ * while requests run.  No counterpart on the attention pages: it exists only so
+ * those callers can run the paged decode.
+ *   Same arguments, layouts and results as attn_decode_paged, without the
+ *   workspace.  The scratch it needs lives in a fixed device array compiled
+ *   into the library (ATTN_NOALLOC_SCRATCH_BYTES, 8 MiB, held on every GPU that
+ *   loads the library until the process exits); sizes whose scratch
+ *   (attn_decode_workspace_size) exceeds it return ATTN_ERR_UNSUPPORTED and
+ *   launch nothing.  It allocates and frees nothing.
+ *   The first call on each device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.  Every call uses the same array: calls whose work overlaps on the
+ *   GPU (different streams, or different host threads on one device) race on it
+ *   and must be ordered by the caller.  No part of the array needs to start at
+ *   zero; each call overwrites what it reads.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                        const int32_t *page_table, const int32_t *seq_lens,
+                                        void *o, float *lse, int B, int Hq, int Hkv, int d,
+                                        int page_size, int num_pages, int max_pages_per_seq,
+                                        float scale, attn_stream_t stream);
+
 /* Library version, e.g. "attn07 0.1.0 sm_103a". */
 const char *attn_version(void);
 
