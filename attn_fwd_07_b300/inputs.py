@@ -212,19 +212,25 @@ WORKLOADS = {
 }
 
 
-def make(name: str):
-    """Generate the named workload's inputs (CPU tensors)."""
+def make(name: str, batch: int | None = None):
+    """Generate the named workload's inputs (CPU tensors).
+
+    ``batch`` replaces the workload's batch size (sequences, for the packed and
+    paged workloads) with the same recipe otherwise; None keeps it."""
     w = WORKLOADS[name]
     p = w.params
     if w.kind == "dense":
-        return dense(p["B"], p["N"], p["Hq"], p["Hkv"], p["d"], w.seed, p["dtype"], p["factor"],
+        B = p["B"] if batch is None else int(batch)
+        return dense(B, p["N"], p["Hq"], p["Hkv"], p["d"], w.seed, p["dtype"], p["factor"],
                      p["causal"])
     if w.kind == "varlen":
-        lens = lengths(p["S"], p["lo"], p["hi"], w.seed)
+        S = p["S"] if batch is None else int(batch)
+        lens = lengths(S, p["lo"], p["hi"], w.seed)
         return varlen(lens, p["Hq"], p["Hkv"], p["d"], w.seed, p["dtype"], p["factor"],
                       p["causal"])
     if w.kind == "decode":
-        lens = lengths(p["B"], p["lo"], p["hi"], w.seed)
+        B = p["B"] if batch is None else int(batch)
+        lens = lengths(B, p["lo"], p["hi"], w.seed)
         maxp = (p["hi"] + p["page_size"] - 1) // p["page_size"]
         return paged(lens, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"], maxp, p["dtype"],
                      p["factor"])

@@ -19,8 +19,13 @@ KV-cache GB/s (4096 bytes per cached token over the decode launches' time).
 Under torchrun every rank runs the same workload (replicas; no data-path
 collective): value = all ranks' FLOPs / max-over-ranks time.
 
+``--workload NAME`` benches one named workload alone (any of the five in
+attn_fwd_07_b300.inputs.WORKLOADS; ``--batch`` replaces its batch size) with the
+same timing rules; when its inputs fit in twice the L2, a 252 MB buffer is
+written between steps to flush it.
+
 ``--impl reference`` times the fp64 CPU oracle on the host cores on bounded
-samples of the same prefill workload (rank 0 only).
+samples of the same workload (rank 0 only).
 """
 from __future__ import annotations
 
@@ -154,25 +159,40 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def library_fingerprint() -> str:
+# the source files each profiled kernel is built from (its own header and the PTX
+# wrappers); a counter taken on other sources no longer describes the kernel
+KERNEL_SOURCES = {
+    "prefill_tc_kernel": ("prefill_tc.cuh", "ptx.cuh"),
+    "prefill_simt_kernel": ("prefill_simt.cuh", "ptx.cuh"),
+    "decode_split_kernel": ("decode.cuh", "ptx.cuh"),
+}
+
+
+def kernel_fingerprint(kernel: str, read=None) -> str:
+    """sha256 (16 hex digits) over the kernel's source files.  `read(name) -> bytes`
+    defaults to the working tree's attn_fwd_07_b300/csrc/<name>."""
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "attn_fwd_07_b300", "csrc", name), "rb") as f:
+                return f.read()
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "attn_fwd_07_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        h.update(read(name))
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if it matches this source."""
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload`, from the committed
+    ncu summary, or None when there is none or it was taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("source_fingerprint") != library_fingerprint():
+        e = d["kernels"]["%s@%s" % (kernel, workload)]
+        if e.get("source_fingerprint") != kernel_fingerprint(kernel):
             return None
-        return d["kernels"][kernel]["dram_bytes_per_launch"]
+        return e["dram_bytes_per_launch"]
     except Exception:
         return None
 
@@ -180,72 +200,235 @@ def profiled_traffic(kernel: str):
 # ---------------------------------------------------------------- workloads
 
 def prefill_flops(w) -> float:
-    B, N, Hq, d = w.q.shape
-    return 2.0 * B * Hq * N * N * d if w.causal else 4.0 * B * Hq * N * N * d
+    """Algorithmic FLOPs of one prefill: 4*d per (query, key) pair (QK^T and PV, 2*d
+    each) over N^2 pairs per sequence and head, halved when causal (2*B*Hq*N^2*d)."""
+    if w.q.dim() == 4:
+        B, N, Hq, d = w.q.shape
+        pairs = B * float(N) * N
+    else:
+        _, Hq, d = w.q.shape
+        lens = w.lens.astype(np.float64)
+        pairs = float((lens * lens).sum())
+    return 4.0 * Hq * d * pairs * (0.5 if w.causal else 1.0)
 
 
 def decode_bytes(w) -> float:
+    """Algorithmic bytes of one decode: each cached token's K and V rows read once."""
     Hkv, d = w.k_cache.shape[2], w.k_cache.shape[3]
-    return 2.0 * Hkv * d * 2.0 * float(w.seq_lens.sum())  # K and V, bf16
+    return 2.0 * Hkv * d * w.k_cache.element_size() * float(w.seq_lens.sum())
 
 
-def cpu_oracle_sample(w, seconds: float, seed: int = 0, rows_per_batch: int = 1024):
-    """Time the fp64 oracle on random query rows of the prefill workload until
-    `seconds` have passed; FLOPs counted like the GPU's (4 * keys * d per row)."""
+def nbytes(*ts) -> int:
+    return int(sum(t.numel() * t.element_size() for t in ts))
+
+
+class Leg:
+    """One workload of the step: device-resident inputs, a launch, its algorithmic work,
+    and an end-to-end variant that copies the inputs in from pinned host memory and the
+    results out."""
+
+    def __init__(self, name, dev, batch=None):
+        import attn_fwd_07_b300 as A
+        from attn_fwd_07_b300 import inputs
+        self.A = A
+        self.name = name
+        self.spec = inputs.WORKLOADS[name]
+        self.kind = self.spec.kind
+        w = inputs.make(name, batch)
+        self.w = w
+        self.scale = w.scale
+        if self.kind == "decode":
+            self.host = [w.q, w.k_cache, w.v_cache, w.page_table, w.seq_lens]
+            self.dev = [t.to(dev) for t in self.host]
+            q, kc = self.dev[0], self.dev[1]
+            B, Hq, d = w.q.shape
+            self.o = torch.empty_like(q)
+            self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+            self.ws = torch.empty(A.attn_decode_workspace_size(B, Hq, kc.shape[2], d,
+                                                               w.page_table.shape[1],
+                                                               kc.shape[1]),
+                                  dtype=torch.uint8, device=dev)
+            self.work, self.unit, self.bound = decode_bytes(w), "GB/s", "hbm"
+            self.kernel = "decode_split_kernel"
+            self.shape = {"B": B, "Hq": Hq, "Hkv": int(kc.shape[2]), "d": d,
+                          "page_size": int(kc.shape[1]),
+                          "total_tokens": int(w.seq_lens.sum())}
+        else:
+            self.host = [w.q, w.k, w.v] + ([w.cu_seqlens] if self.kind == "varlen" else [])
+            self.dev = [t.to(dev) for t in self.host]
+            q = self.dev[0]
+            self.o = torch.empty_like(q)
+            if self.kind == "varlen":
+                T, Hq, d = w.q.shape
+                self.max_len = int(w.lens.max())
+                self.lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+                self.shape = {"seqs": len(w.lens), "total_tokens": T, "Hq": Hq,
+                              "Hkv": int(w.k.shape[1]), "d": d, "causal": w.causal}
+            else:
+                B, N, Hq, d = w.q.shape
+                self.lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+                self.shape = {"B": B, "N": N, "Hq": Hq, "Hkv": int(w.k.shape[2]), "d": d,
+                              "causal": w.causal}
+            self.f32 = w.q.dtype == torch.float32
+            self.work, self.unit = prefill_flops(w), "TFLOP/s"
+            self.bound = "alu" if self.f32 else "tensor"
+            self.kernel = "prefill_simt_kernel" if self.f32 else "prefill_tc_kernel"
+        self.shape["values"] = self.spec.description
+        self.h2d = nbytes(*self.host)
+        self.d2h = nbytes(self.o, self.lse)
+
+    def launch(self, stream):
+        A, d = self.A, self.dev
+        if self.kind == "decode":
+            A.attn_decode_paged(d[0], d[1], d[2], d[3], d[4], self.scale, o=self.o, lse=self.lse,
+                                workspace=self.ws, stream=stream)
+        elif self.kind == "varlen":
+            A.attn_fwd_varlen(d[0], d[1], d[2], d[3], self.max_len, self.w.causal, self.scale,
+                              o=self.o, lse=self.lse, stream=stream)
+        elif self.f32:
+            A.attn_fwd_f32(d[0], d[1], d[2], self.w.causal, self.scale, o=self.o, lse=self.lse,
+                           stream=stream)
+        else:
+            A.attn_fwd(d[0], d[1], d[2], self.w.causal, self.scale, o=self.o, lse=self.lse,
+                       stream=stream)
+
+    def rate(self, work, ms):
+        """work units (FLOPs or bytes) over ms -> TFLOP/s or GB/s."""
+        return work / (ms * 1e-3) / (1e12 if self.unit == "TFLOP/s" else 1e9)
+
+    def e2e_setup(self):
+        self.h_in = [t.pin_memory() for t in self.host]
+        self.h_out = [torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory(),
+                      torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()]
+
+    def e2e_step(self, stream):
+        for dst, src in zip(self.dev, self.h_in):
+            dst.copy_(src, non_blocking=True)
+        self.launch(stream)
+        self.h_out[0].copy_(self.o, non_blocking=True)
+        self.h_out[1].copy_(self.lse, non_blocking=True)
+
+    def e2e_teardown(self):
+        del self.h_in, self.h_out
+
+
+def launches_per_call(leg) -> int:
+    return 2 if leg.kind == "decode" else 1
+
+
+def cpu_oracle_sample(w, kind: str, seconds: float, seed: int = 0):
+    """Time the fp64 oracle on random pieces of a workload until `seconds` have passed.
+
+    Prefill (dense or packed): batches of random query rows, each counted like the GPU's
+    work (4*d FLOPs per allowed key).  Decode: random whole sequences, counted as their
+    K and V bytes.  Returns (rate in TFLOP/s or GB/s, elapsed s, description, threads)."""
     from oracle import oracle
-    q, k, v = (t.float().numpy() for t in (w.q, w.k, w.v))
-    B, N, Hq, d = w.q.shape
     rng = np.random.default_rng(seed)
-    flops, rows_done, t0 = 0.0, 0, time.perf_counter()
+    work, done, t0 = 0.0, 0, time.perf_counter()
+    if kind == "decode":
+        arrs = [t.float().numpy() for t in (w.q, w.k_cache, w.v_cache)]
+        pt, sl = w.page_table.numpy(), w.seq_lens.numpy()
+        Hkv, d = w.k_cache.shape[2], w.k_cache.shape[3]
+        t0 = time.perf_counter()
+        while True:
+            b = int(rng.integers(0, len(sl)))
+            oracle.decode_paged(*arrs, pt, sl, w.scale, seqs=[b])
+            work += 2.0 * Hkv * d * 2.0 * float(sl[b])
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return work / el / 1e9, el, "%d random sequences (%.1f s, fp64)" % (done, el), \
+                    oracle.max_threads()
+    if w.q.dim() == 4:
+        segs = [(w.q.float().numpy(), w.k.float().numpy(), w.v.float().numpy())]
+    else:  # packed: each sequence as a batch-1 dense problem
+        cu = w.cu_seqlens.numpy()
+        q, k, v = (t.float().numpy() for t in (w.q, w.k, w.v))
+        segs = [(q[None, a:b], k[None, a:b], v[None, a:b]) for a, b in zip(cu[:-1], cu[1:])
+                if b > a]
+    n_rows = 1024
+    t0 = time.perf_counter()
     while True:
-        rows = np.stack([rng.integers(0, B, rows_per_batch), rng.integers(0, Hq, rows_per_batch),
-                         rng.integers(0, N, rows_per_batch)], 1).astype(np.int32)
+        q, k, v = segs[int(rng.integers(0, len(segs)))]
+        B, N, Hq, d = q.shape
+        rows = np.stack([rng.integers(0, B, n_rows), rng.integers(0, Hq, n_rows),
+                         rng.integers(0, N, n_rows)], 1).astype(np.int32)
         oracle.attn_rows(q, k, v, rows, w.causal, w.scale)
-        keys = (rows[:, 2].astype(np.float64) + 1.0) if w.causal else np.full(len(rows), N, float)
-        flops += float(4.0 * keys.sum() * d)
-        rows_done += len(rows)
+        keys = (rows[:, 2].astype(np.float64) + 1.0) if w.causal else np.full(n_rows, float(N))
+        work += float(4.0 * keys.sum() * d)
+        done += n_rows
         el = time.perf_counter() - t0
         if el >= seconds:
-            break
-    return flops / el / 1e12, el, rows_done, oracle.max_threads()
+            return work / el / 1e12, el, "%d random query rows (%.1f s, fp64)" % (done, el), \
+                oracle.max_threads()
 
 
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
+    """The fp64 oracle, as it stands, on the host cores: each step a bounded sample of
+    the same workloads, same metric and units as the GPU arm (value = the first
+    workload's rate; the default step's decode leg is reported beside it)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     from attn_fwd_07_b300 import inputs
-    w = inputs.make(PREFILL)
-    per_step = max(0.5, args.ref_seconds / max(1, args.steps))
-    for _ in range(args.warmup):
-        cpu_oracle_sample(w, 0.05)
-    vals, els, rows = [], 0.0, 0
-    for s in range(args.steps):
-        tf, el, r, cores = cpu_oracle_sample(w, per_step, seed=s + 1)
-        vals.append(tf)
-        els += el
-        rows += r
-    value = float(np.mean(vals))
+    names = [args.workload] if args.workload else [PREFILL, DECODE]
+    per_step = max(0.5, args.ref_seconds / max(1, args.steps) / len(names))
+    results = []
+    for name in names:
+        kind = inputs.WORKLOADS[name].kind
+        w = inputs.make(name, args.batch)
+        for _ in range(args.warmup):
+            cpu_oracle_sample(w, kind, 0.05)
+        vals, els, descs, cores = [], 0.0, [], 0
+        for s in range(args.steps):
+            v, el, desc, cores = cpu_oracle_sample(w, kind, per_step, seed=s + 1)
+            vals.append(v)
+            els += el
+            descs.append(desc)
+        unit = "GB/s" if kind == "decode" else "TFLOP/s"
+        results.append((name, kind, float(np.mean(vals)), unit, els, descs[0], cores))
+    name, kind, value, unit, els, desc, cores = results[0]
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * els / max(1, args.steps), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": PREFILL, "B": 1, "Hq": 32, "Hkv": 8, "N": 16384, "d": 128,
-                   "causal": True, "parallelism": "replicas", "l2": "not applicable (CPU)"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "%d random causal query rows of the prefill workload over %d "
-                                   "steps (%.1f s)" % (rows, args.steps, els)},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "ms_per_step": 1000.0 * sum(r[4] for r in results) / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": " + ".join(names), "batch_override": args.batch,
+                   "parallelism": "single process", "l2": "not applicable (CPU)"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": "per step: %s; %d steps" % (desc, args.steps)},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    for name, kind, v, u, els, desc, cores in results[1:]:
+        line[kind] = {"value": v, "unit": u, "sample": "per step: " + desc}
     print(json.dumps(line), flush=True)
     return 0
 
 
 # ---------------------------------------------------------------- our arm
+
+L2_BYTES = 126 * 1024 * 1024
+
+
+def roofline(leg, launch_ms, peaks, peak_src):
+    if leg.bound == "alu":
+        return None  # fp32 CUDA-core path: launch-latency bound at its workload
+    if leg.bound == "tensor":
+        r = {"bound": "tensor", "achieved": leg.rate(leg.work, launch_ms),
+             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+             "peak_source": "%s bf16 burst (cuBLAS)" % peak_src}
+    else:
+        r = {"bound": "hbm", "achieved": leg.rate(leg.work, launch_ms),
+             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+             "peak_source": "%s copy bandwidth" % peak_src}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["traffic"] = profiled_traffic(leg.kernel, leg.name)
+    return r
+
 
 def run_gpu(args):
     world, rank = dist_init("nccl")
@@ -253,37 +436,26 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     import attn_fwd_07_b300 as A
-    from attn_fwd_07_b300 import inputs
     A.load_library()
 
-    # ---- inputs (host, seeded) -> device
-    wp = inputs.make(PREFILL)
-    wd = inputs.make(DECODE)
-    qp, kp, vp = (t.to(dev) for t in (wp.q, wp.k, wp.v))
-    B, N, Hq, d = wp.q.shape
-    op = torch.empty_like(qp)
-    lsep = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-    qd, kc, vc, pt, sl = (t.to(dev) for t in (wd.q, wd.k_cache, wd.v_cache, wd.page_table,
-                                               wd.seq_lens))
-    od = torch.empty_like(qd)
-    lsed = torch.empty(qd.shape[:2], dtype=torch.float32, device=dev)
-    Bd, Hqd, dd = wd.q.shape
-    ws = torch.empty(A.attn_decode_workspace_size(Bd, Hqd, kc.shape[2], dd, pt.shape[1],
-                                                  kc.shape[1]), dtype=torch.uint8, device=dev)
+    names = [args.workload] if args.workload else [PREFILL, DECODE]
+    legs = [Leg(n, dev, args.batch) for n in names]
     stream = torch.cuda.current_stream(dev)
-    fl_p = prefill_flops(wp)
-    by_d = decode_bytes(wd)
+    resident = sum(nbytes(*leg.dev, leg.o, leg.lse) for leg in legs)
+    flush = None
+    if resident < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    nl = len(legs)
 
     def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        A.attn_fwd(qp, kp, vp, True, wp.scale, o=op, lse=lsep, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        A.attn_decode_paged(qd, kc, vc, pt, sl, wd.scale, o=od, lse=lsed, workspace=ws,
-                            stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
+        if flush is not None:
+            flush.zero_()
+        for i, leg in enumerate(legs):
+            if ev is not None:
+                ev[i][0].record(stream)
+            leg.launch(stream)
+            if ev is not None:
+                ev[i][1].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -292,17 +464,14 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError("device status after warm-up: " + A.attn_status_string(st))
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t_begin = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nl)]
+           for _ in range(args.steps)]
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
-    t_begin.record(stream)
     for s in range(args.steps):
         step(evs[s])
-    t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
@@ -310,118 +479,68 @@ def run_gpu(args):
     if st != 0:
         raise RuntimeError("device status after timing: " + A.attn_status_string(st))
 
-    total_ms = t_begin.elapsed_time(t_end)
-    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    pre_sum = max_over_ranks(sum(pre_ms), world, dev)
-    dec_sum = max_over_ranks(sum(dec_ms), world, dev)
-    total_ms = max_over_ranks(total_ms, world, dev)
-    value = sum_over_ranks(fl_p * args.steps, world, dev) / (pre_sum * 1e-3) / 1e12
-    dec_gbs = sum_over_ranks(by_d * args.steps, world, dev) / (dec_sum * 1e-3) / 1e9
+    leg_ms = [max_over_ranks(sum(evs[s][i][0].elapsed_time(evs[s][i][1])
+                                 for s in range(args.steps)), world, dev) for i in range(nl)]
+    leg_val = [legs[i].rate(sum_over_ranks(legs[i].work * args.steps, world, dev), leg_ms[i])
+               for i in range(nl)]
 
-    # ---- end to end through the public API with host buffers (pinned), copies timed
+    # ---- end to end through the public API: pinned host inputs in, results out, timed
     n_e2e = max(1, min(args.steps, args.e2e_steps))
-    hq, hk, hv = (t.pin_memory() for t in (wp.q, wp.k, wp.v))
-    ho, hl = torch.empty_like(hq).pin_memory(), torch.empty(lsep.shape, dtype=torch.float32).pin_memory()
-    h2d_p = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h_p = ho.numel() * ho.element_size() + hl.numel() * 4
-
-    def e2e_prefill():
-        qp.copy_(hq, non_blocking=True)
-        kp.copy_(hk, non_blocking=True)
-        vp.copy_(hv, non_blocking=True)
-        A.attn_fwd(qp, kp, vp, True, wp.scale, o=op, lse=lsep, stream=stream)
-        ho.copy_(op, non_blocking=True)
-        hl.copy_(lsep, non_blocking=True)
-
-    e2e_prefill()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n_e2e):
-        e2e_prefill()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
-    e2e_val = sum_over_ranks(fl_p * n_e2e, world, dev) / (e2e_ms * 1e-3) / 1e12
-    del hq, hk, hv, ho, hl
-
-    hqd, hkc, hvc, hpt, hsl = (t.pin_memory() for t in (wd.q, wd.k_cache, wd.v_cache,
-                                                        wd.page_table, wd.seq_lens))
-    hod = torch.empty_like(hqd).pin_memory()
-    hld = torch.empty(lsed.shape, dtype=torch.float32).pin_memory()
-    h2d_d = sum(t.numel() * t.element_size() for t in (hqd, hkc, hvc, hpt, hsl))
-    d2h_d = hod.numel() * hod.element_size() + hld.numel() * 4
-
-    def e2e_decode():
-        for dst, src in ((qd, hqd), (kc, hkc), (vc, hvc), (pt, hpt), (sl, hsl)):
-            dst.copy_(src, non_blocking=True)
-        A.attn_decode_paged(qd, kc, vc, pt, sl, wd.scale, o=od, lse=lsed, workspace=ws,
-                            stream=stream)
-        hod.copy_(od, non_blocking=True)
-        hld.copy_(lsed, non_blocking=True)
-
-    e2e_decode()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    a.record(stream)
-    for _ in range(n_e2e):
-        e2e_decode()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_dms = max_over_ranks(a.elapsed_time(b), world, dev)
-    e2e_dval = sum_over_ranks(by_d * n_e2e, world, dev) / (e2e_dms * 1e-3) / 1e9
-    del hqd, hkc, hvc, hpt, hsl, hod, hld
+    e2e = []
+    for leg in legs:
+        leg.e2e_setup()
+        leg.e2e_step(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            leg.e2e_step(stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e.append({"value": leg.rate(sum_over_ranks(leg.work * n_e2e, world, dev), ms),
+                    "unit": leg.unit, "h2d_bytes_per_step": leg.h2d,
+                    "d2h_bytes_per_step": leg.d2h})
+        leg.e2e_teardown()
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only)
     cpu = None
+    p0 = legs[0]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, el, rows, cores = cpu_oracle_sample(wp, args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": "%d random causal query rows of the prefill workload (%.1f s, fp64)"
-                         % (rows, el)}
+        v, el, desc, cores = cpu_oracle_sample(p0.w, p0.kind, args.cpu_seconds)
+        cpu = {"value": v, "unit": p0.unit, "cores": cores, "kind": "oracle", "sample": desc}
 
     peaks, peak_src = load_peaks()
-    pre_launch_ms = pre_sum / args.steps
-    dec_launch_ms = dec_sum / args.steps
-    roof_p = {"bound": "tensor", "achieved": fl_p / (pre_launch_ms * 1e-3) / 1e12,
-              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-              "peak_source": "%s bf16 burst (cuBLAS)" % peak_src,
-              "traffic": profiled_traffic("prefill_tc_kernel")}
-    roof_p["frac"] = roof_p["achieved"] / roof_p["peak"]
-    roof_d = {"bound": "hbm", "achieved": by_d / (dec_launch_ms * 1e-3) / 1e9,
-              "peak": peaks["hbm_gbs"], "unit": "GB/s",
-              "peak_source": "%s copy bandwidth" % peak_src,
-              "traffic": profiled_traffic("decode_split_kernel")}
-    roof_d["frac"] = roof_d["achieved"] / roof_d["peak"]
+    roofs = [roofline(legs[i], leg_ms[i] / args.steps, peaks, peak_src) for i in range(nl)]
 
     if rank == 0:
+        l2 = ("inputs larger than L2 (%.2f GB resident)" % (resident / 1e9) if flush is None
+              else "L2 flushed between steps (%d MB buffer written)" % (flush.numel() >> 20))
+        config = {"workload": " + ".join(names), "batch_override": args.batch,
+                  "parallelism": "replicas" if world > 1 else "single GPU", "l2": l2}
+        for leg in legs:
+            config[leg.kind if leg.kind != "dense" else "prefill"] = dict(leg.shape,
+                                                                           name=leg.name)
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": "%s + %s" % (PREFILL, DECODE), "prefill": {
-                "B": B, "Hq": Hq, "Hkv": int(kp.shape[2]), "N": N, "d": d, "causal": True,
-                "values": "bf16 N(0,1)*0.5"},
-                "decode": {"B": Bd, "Hq": Hqd, "Hkv": int(kc.shape[2]), "d": dd,
-                           "page_size": int(kc.shape[1]), "lengths": "U[1024,32768]",
-                           "total_tokens": int(wd.seq_lens.sum())},
-                "parallelism": "replicas" if world > 1 else "single GPU",
-                "l2": "inputs larger than L2 (prefill 335 MB, decode %.1f GB)" % (by_d / 1e9)},
-            "roofline": roof_p,
-            "decode": {"value": dec_gbs, "unit": "GB/s", "ms_per_step": dec_sum / args.steps,
-                       "roofline": roof_d,
-                       "e2e": {"value": e2e_dval, "unit": "GB/s", "h2d_bytes_per_step": h2d_d,
-                               "d2h_bytes_per_step": d2h_d}},
-            "prefill_ms_per_step": pre_sum / args.steps,
-            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d_p,
-                    "d2h_bytes_per_step": d2h_p},
+            "metric": METRIC, "value": leg_val[0], "unit": p0.unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sum(leg_ms) / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if getattr(p0, "f32", False) else "bf16", "data": "synthetic",
+            "config": config,
+            "roofline": roofs[0],
+            "e2e": e2e[0],
             "cpu_baseline": cpu,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": args.steps * sum(launches_per_call(leg) for leg in legs),
             "clocks": clocks,
         }
+        line["%s_ms_per_step" % ("decode" if p0.kind == "decode" else "prefill")] = \
+            leg_ms[0] / args.steps
+        for i in range(1, nl):
+            line[legs[i].kind] = {"value": leg_val[i], "unit": legs[i].unit,
+                                  "ms_per_step": leg_ms[i] / args.steps,
+                                  "roofline": roofs[i], "e2e": e2e[i]}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -434,6 +553,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["attn07", "reference"], default="attn07")
+    ap.add_argument("--workload", default=None,
+                    help="bench one named workload alone (attn_fwd_07_b300.inputs.WORKLOADS) "
+                         "instead of the default prefill + decode step")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="replace the workload's batch size (sequences) with this one")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
@@ -441,6 +565,11 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload is not None:
+        from attn_fwd_07_b300 import inputs
+        if args.workload not in inputs.WORKLOADS:
+            ap.error("unknown workload %r; one of %s" % (args.workload,
+                                                         ", ".join(inputs.WORKLOADS)))
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
