@@ -132,15 +132,21 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.ntiles = ntiles;
+    // a CTA takes two query heads of one group on the same rows when the group size is
+    // even, else two consecutive row tiles of one head
+    p.head_pairs = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = scale * kLog2e;
-    const long long grid = (long long)ntiles * Hq * nseq;
+    const long long grid = p.head_pairs ? (long long)ntiles * (Hq / 2) * nseq
+                                        : (long long)((ntiles + 1) / 2) * Hq * nseq;
     if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     if (grid == 0) return ATTN_OK;
     if (d == 128) {
-        prefill_tc_kernel<128><<<(unsigned)grid, 192, PrefillCfg<128>::SMEM, stream>>>(p, mq, mk, mv);
+        prefill_tc_kernel<128><<<(unsigned)grid, PrefillCfg<128>::THREADS, PrefillCfg<128>::SMEM,
+                                 stream>>>(p, mq, mk, mv);
     } else {
-        prefill_tc_kernel<64><<<(unsigned)grid, 192, PrefillCfg<64>::SMEM, stream>>>(p, mq, mk, mv);
+        prefill_tc_kernel<64><<<(unsigned)grid, PrefillCfg<64>::THREADS, PrefillCfg<64>::SMEM,
+                                stream>>>(p, mq, mk, mv);
     }
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

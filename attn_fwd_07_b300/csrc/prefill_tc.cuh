@@ -7,34 +7,45 @@
 // (section "FlashAttention'ın Temelleri"), with the online softmax of section
 // "Online Softmax Prensibi" (running row maximum M and sum L), so the N x N
 // score matrix never reaches device memory.  As in section "FlashAttention-2:
-// Optimizasyonlar ve İyileştirmeler", each CTA owns a block of 128 query rows
-// of one (sequence, query head) and streams all of that head's keys and values,
-// loading the next block while the current one is computed.
+// Optimizasyonlar ve İyileştirmeler", work is split over blocks of query rows
+// that each stream all the keys and values they need, loading the next block
+// while the current one is computed.
 //
-// Work of one CTA (one 128-row query tile):
-//   warp 4  (TMA)      loads the Q tile once, then K_j and V_j (128 keys each)
-//                      into two 3-stage shared-memory rings (128-byte swizzle)
-//   warp 5  (MMA)      one thread issues tcgen05.mma:
-//                        S_j = Q K_j^T       (128x128, K = d) into TMEM buffer j%2
-//                        O  += P_j V_j       (P_j read from TMEM, 128 x d, K = 128)
-//                      issuing S_{j+1} before waiting for P_j, so the tensor core
-//                      computes the next scores while the softmax warps work
-//   warps 0-3 (softmax) one thread per query row: load the row of S_j from TMEM,
-//                      mask (causal diagonal / sequence end), update the running
-//                      maximum, P = 2^(S*scale*log2e - M) rounded to bf16, add the
-//                      row sum of the rounded P into L, write P into TMEM, then the
-//                      epilogue O / L -> bf16.
+// One CTA owns two 128-row query tiles that share one key/value head: two
+// query heads of the same group on the same rows when the group size is even,
+// else two consecutive row tiles of one head.  Both tiles use every K_j and
+// V_j tile loaded into shared memory, which halves the load traffic per MMA,
+// and the two tiles' softmax runs while the tensor core works on the other
+// tile ("ping-pong").
 //
-// Rescaling: the row maximum used for the exponent is only moved when the new
+// Warp roles (384 threads):
+//   warps 0-3   softmax of tile 0, one thread per query row (TMEM lane)
+//   warps 4-7   softmax of tile 1
+//   warp 8      TMA producer: both Q tiles once, then K_j / V_j (128 keys)
+//               into two shared-memory rings (128-byte swizzle)
+//   warp 9      MMA issuer (one thread), in this order for every j:
+//                  O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,
+//                  O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
+//               tcgen05.mma ops of one thread execute in issue order, so
+//               S_{j+1} never overwrites P_j before O += P_j V_j has read it,
+//               and a commit after S_{j+1} also covers that PV product.
+//   warps 10-11 idle (they complete the third warpgroup)
+//
+// Softmax step for tile t and key tile j (thread = row): load the S row from
+// TMEM, mask (causal diagonal / sequence end), running maximum, P = 2^(S *
+// scale * log2e - M) rounded to bf16 and written back over the S columns it
+// came from (P is the A operand of the PV product, read from TMEM), row sums.
+//
+// Rescaling: the row maximum used in the exponent only moves when the new
 // maximum exceeds it by more than 8 (log2 units).  Until then P may reach
-// 2^8, which fp32 and bf16 hold exactly in range; the output and the sum are
-// always scaled consistently, so the result is the same exact softmax.  When it
-// moves, O (in TMEM) and L are multiplied by 2^(M_old - M_new), which is the
+// 2^8, which fp32 and bf16 hold exactly in range; output and sums are always
+// scaled consistently, so the result is the same exact softmax.  When it
+// moves, O (in TMEM) and the sums are multiplied by 2^(M_old - M_new): the
 // output rescaling that accompanies the online softmax.
 //
 // Tensor memory (512 columns of 128 lanes x 32 bit):
-//   [0,128) S buffer 0, [128,256) S buffer 1, [256,256+d) O,
-//   [384,448) P buffer 0, [448,512) P buffer 1 (128 bf16 per row, packed in pairs)
+//   [0,128) S_0 (P_0 in its first 64 columns), [128,256) S_1 / P_1,
+//   [256,256+d) O_0, [384,384+d) O_1
 #pragma once
 
 #include "ptx.cuh"
@@ -50,7 +61,8 @@ struct PrefillParams {
     int nseq;       // dense: B; varlen: num_seqs
     int total;      // varlen: total tokens
     int Hq, Hkv;
-    int ntiles;     // query tiles per sequence (of the longest sequence)
+    int ntiles;     // 128-row query tiles per sequence (of the longest sequence)
+    int head_pairs; // 1: a CTA takes two heads of a group on the same rows; 0: two row tiles
     int causal;
     float scale_log2;
 };
@@ -63,16 +75,16 @@ struct PrefillCfg {
     static constexpr uint32_t HALF = 128u * 128u;         // one [128 rows][64] bf16 half: 16 KB
     static constexpr uint32_t TILE = NH * HALF;
     static constexpr int SK = (D == 128) ? 3 : 4;         // K ring stages
-    static constexpr int SV = SK;                         // V ring stages
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = TILE;
+    static constexpr int SV = (D == 128) ? 2 : 4;         // V ring stages
+    static constexpr uint32_t OFF_Q = 0;                  // Q_0, Q_1
+    static constexpr uint32_t OFF_K = 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + SK * TILE;
     static constexpr uint32_t OFF_CTRL = OFF_V + SV * TILE;
     static constexpr uint32_t CTRL_BYTES = 512;
     static constexpr size_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
     // TMEM columns
-    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_P0 = 384, COL_P1 = 448;
-    static constexpr int THREADS = 192;
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
+    static constexpr int THREADS = 384;
 };
 
 // barrier slots inside the control block (8 bytes each)
@@ -82,28 +94,29 @@ enum : uint32_t {
     BAR_KEMPTY = 5,   // +s
     BAR_VFULL = 9,    // +s
     BAR_VEMPTY = 13,  // +s
-    BAR_SFULL = 17,   // +b, b < 2
-    BAR_SEMPTY = 19,
-    BAR_PFULL = 21,
-    BAR_PVDONE = 23,
-    BAR_DRAIN = 25,
-    BAR_COUNT = 26
+    BAR_SFULL = 17,   // +t, t < 2
+    BAR_PFULL = 19,   // +t
+    BAR_OFULL = 21,   // +t
+    BAR_DRAIN = 23,
+    BAR_COUNT = 24
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t pf_smem_raw[];
 
-    // ---- work item: heaviest query tiles first, heads fastest
-    const int units = p.Hq * p.nseq;
-    const int tile = p.ntiles - 1 - (int)(blockIdx.x / units);
+    // ---- work item: heaviest query tiles first, heads fastest (a key/value head's
+    //      query heads run together and share its K/V tiles in L2)
+    const int hunits = p.head_pairs ? p.Hq / 2 : p.Hq;
+    const int units = hunits * p.nseq;
+    const int nouter = p.head_pairs ? p.ntiles : (p.ntiles + 1) / 2;
+    const int outer = nouter - 1 - (int)(blockIdx.x / units);
     const int rem = (int)(blockIdx.x % units);
-    const int h = rem % p.Hq;
-    const int sq = rem / p.Hq;
-    const int g = h / (p.Hq / p.Hkv);
+    const int hu = rem % hunits;
+    const int sq = rem / hunits;
     int tok0, len, batch;
     if (p.cu_seqlens) {
         tok0 = p.cu_seqlens[sq];
@@ -114,9 +127,25 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         len = p.N;
         batch = sq;
     }
-    if (tile < 0 || tile * C::BM >= len) return;  // uniform: nothing to do
+    // the CTA's two tiles: query head and first row of each
+    int head[2], row0[2], nt[2];
+    if (p.head_pairs) {
+        head[0] = 2 * hu;
+        head[1] = 2 * hu + 1;
+        row0[0] = row0[1] = outer * C::BM;
+    } else {
+        head[0] = head[1] = hu;
+        row0[0] = 2 * outer * C::BM;
+        row0[1] = row0[0] + C::BM;
+    }
+    const int g = head[0] / (p.Hq / p.Hkv);
     const int nkv_all = (len + C::BN - 1) / C::BN;
-    const int n_kv = p.causal ? min(tile + 1, nkv_all) : nkv_all;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        nt[t] = (outer < 0 || row0[t] >= len) ? 0
+                : (p.causal ? min(row0[t] / C::BN + 1, nkv_all) : nkv_all);
+    if (nt[0] == 0 && nt[1] == 0) return;  // uniform: nothing to do
+    const int n_kv = max(nt[0], nt[1]);
 
     const uint32_t raw = smem_u32(pf_smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -130,7 +159,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 128) {
+    if (threadIdx.x == 256) {
         mbar_init(bar(BAR_Q), 1);
         for (int s = 0; s < C::SK; ++s) {
             mbar_init(bar(BAR_KFULL + s), 1);
@@ -140,17 +169,16 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             mbar_init(bar(BAR_VFULL + s), 1);
             mbar_init(bar(BAR_VEMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(BAR_SFULL + b), 1);
-            mbar_init(bar(BAR_SEMPTY + b), 4);
-            mbar_init(bar(BAR_PFULL + b), 4);
-            mbar_init(bar(BAR_PVDONE + b), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(BAR_SFULL + t), 1);
+            mbar_init(bar(BAR_PFULL + t), 4);
+            mbar_init(bar(BAR_OFULL + t), 1);
         }
         mbar_init(bar(BAR_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(ctrl + 8 * BAR_COUNT, 512);
         tmem_relinquish();
     }
@@ -159,7 +187,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ============================ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmQ);
@@ -167,12 +195,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             prefetch_tmap(&tmV);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            const int qrow = tok0 + tile * C::BM;
-            mbar_arrive_expect_tx(bar(BAR_Q), C::TILE);
+            mbar_arrive_expect_tx(bar(BAR_Q), (uint32_t)((nt[0] > 0) + (nt[1] > 0)) * C::TILE);
 #pragma unroll
-            for (int hf = 0; hf < C::NH; ++hf)
-                tma_load_4d(base + C::OFF_Q + hf * C::HALF, &tmQ, bar(BAR_Q), hf * 64, h, qrow,
-                            batch, pol_q);
+            for (int t = 0; t < 2; ++t) {
+                if (nt[t] == 0) continue;
+#pragma unroll
+                for (int hf = 0; hf < C::NH; ++hf)
+                    tma_load_4d(base + C::OFF_Q + t * C::TILE + hf * C::HALF, &tmQ, bar(BAR_Q),
+                                hf * 64, head[t], tok0 + row0[t], batch, pol_q);
+            }
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < n_kv; ++j) {
                 const int kvrow = tok0 + j * C::BN;
@@ -208,99 +239,121 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 mbar_wait(bar(BAR_Q), 0u, p.status, nullptr);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ============================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, 64, 0, 1);
-            bool ok = mbar_wait(bar(BAR_Q), 0u, p.status, abort_flag);
-            auto issue_qk = [&](int j) -> bool {
-                const int sk = j % C::SK;
-                const int sb = j & 1;
-                if (!mbar_wait(bar(BAR_KFULL + sk), (uint32_t)(j / C::SK) & 1u, p.status,
-                               abort_flag))
-                    return false;
-                if (!mbar_wait(bar(BAR_SEMPTY + sb), ((uint32_t)(j >> 1) & 1u) ^ 1u, p.status,
-                               abort_flag))
-                    return false;
-                tc_fence_after();
-                const uint32_t qb = base + C::OFF_Q;
-                const uint32_t kb = base + C::OFF_K + sk * C::TILE;
-                const uint32_t dcol = tmem + (sb ? C::COL_S1 : C::COL_S0);
+            // S_t = Q_t K_j^T into S buffer t
+            auto issue_qk = [&](int t, int j) {
+                const uint32_t qb = base + C::OFF_Q + t * C::TILE;
+                const uint32_t kb = base + C::OFF_K + (j % C::SK) * C::TILE;
+                const uint32_t dcol = tmem + (t ? C::COL_S1 : C::COL_S0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (uint32_t)(kk >> 2) * C::HALF + (uint32_t)(kk & 3) * 32u;
                     tc_mma_ss(dcol, smem_desc_sw128(qb + off, 1024, 1024),
                               smem_desc_sw128(kb + off, 1024, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(BAR_SFULL + sb));
-                tc_commit(bar(BAR_KEMPTY + sk));
-                return true;
+                tc_commit(bar(BAR_SFULL + t));
             };
-            if (ok) ok = issue_qk(0);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv && !issue_qk(j + 1)) break;
-                const int sb = j & 1;
-                const int sv = j % C::SV;
-                if (!mbar_wait(bar(BAR_PFULL + sb), (uint32_t)(j >> 1) & 1u, p.status, abort_flag))
-                    break;
-                if (!mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u, p.status,
-                               abort_flag))
-                    break;
+            bool ok = mbar_wait(bar(BAR_Q), 0u, p.status, abort_flag) &&
+                      mbar_wait(bar(BAR_KFULL + 0), 0u, p.status, abort_flag);
+            if (ok) {
                 tc_fence_after();
-                const uint32_t vb = base + C::OFF_V + sv * C::TILE;
-                const uint32_t pcol = tmem + (sb ? C::COL_P1 : C::COL_P0);
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk) {
+                for (int t = 0; t < 2; ++t)
+                    if (nt[t] > 0) issue_qk(t, 0);
+                tc_commit(bar(BAR_KEMPTY + 0));
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int sv = j % C::SV;
+                const int sk1 = (j + 1) % C::SK;
+                bool v_ready = false, k_ready = false;
 #pragma unroll
-                    for (int hf = 0; hf < C::NH; ++hf) {
-                        tc_mma_ts(tmem + C::COL_O + hf * 64, pcol + kk * 8,
-                                  smem_desc_sw128(vb + hf * C::HALF + kk * 2048u, 1024, 1024),
-                                  idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int t = 0; t < 2; ++t) {
+                    if (j >= nt[t]) continue;
+                    if (!mbar_wait(bar(BAR_PFULL + t), (uint32_t)j & 1u, p.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!v_ready) {
+                        if (!mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u, p.status,
+                                       abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        v_ready = true;
+                    }
+                    tc_fence_after();
+                    // O_t += P_t V_j: P_t (bf16, 128 x 128) from the S_t columns of TMEM
+                    const uint32_t vb = base + C::OFF_V + sv * C::TILE;
+                    const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
+                    const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
+#pragma unroll
+                    for (int kk = 0; kk < C::BN / 16; ++kk) {
+#pragma unroll
+                        for (int hf = 0; hf < C::NH; ++hf) {
+                            tc_mma_ts(ocol + hf * 64, pcol + kk * 8,
+                                      smem_desc_sw128(vb + hf * C::HALF + kk * 2048u, 1024, 1024),
+                                      idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    if (j + 1 < nt[t]) {
+                        if (!k_ready) {
+                            if (!mbar_wait(bar(BAR_KFULL + sk1), (uint32_t)((j + 1) / C::SK) & 1u,
+                                           p.status, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            k_ready = true;
+                            tc_fence_after();
+                        }
+                        issue_qk(t, j + 1);
+                    } else {
+                        tc_commit(bar(BAR_OFULL + t));
                     }
                 }
-                tc_commit(bar(BAR_PVDONE + sb));
+                if (!ok) break;
                 tc_commit(bar(BAR_VEMPTY + sv));
+                if (k_ready) tc_commit(bar(BAR_KEMPTY + sk1));
             }
             // all issued MMAs complete before TMEM is released
             tc_commit(bar(BAR_DRAIN));
             mbar_wait(bar(BAR_DRAIN), 0u, p.status, nullptr);
         }
-    } else {
-        // ============================ softmax warps 0-3: thread = query row
-        const int r = threadIdx.x;                 // row in tile, 0..127
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const int qpos = tile * C::BM + r;         // position within the sequence
+    } else if (warp < 8) {
+        // ============================ softmax: warpgroup t, thread = query row
+        const int t = warp >> 2;
+        const int n_mine = t ? nt[1] : nt[0];
+        const int r = threadIdx.x & 127;           // row in tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t scol = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
+        const uint32_t ocol = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
+        const int qpos = (t ? row0[1] : row0[0]) + r;  // position within the sequence
+        const int lim = p.causal ? min(len - 1, qpos) : (len - 1);  // last allowed key
         float m_ref = -INFINITY;                   // log2 units, scaled
         float l = 0.f;                             // sum of P (fp32) -> LSE
         float lr = 0.f;                            // sum of bf16-rounded P -> normalises O
         const float sl2 = p.scale_log2;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int sb = j & 1;
-            ok = mbar_wait(bar(BAR_SFULL + sb), (uint32_t)(j >> 1) & 1u, p.status, abort_flag);
+        for (int j = 0; j < n_mine; ++j) {
+            ok = mbar_wait(bar(BAR_SFULL + t), (uint32_t)j & 1u, p.status, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t sr[128];
-            const uint32_t scol = tmem + lane_base + (sb ? C::COL_S1 : C::COL_S0);
             tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
             tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
             tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
             tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_SEMPTY + sb));
 
             float *s = reinterpret_cast<float *>(sr);
             const int kv0 = j * C::BN;
-            const bool tail = kv0 + C::BN > len;
-            const bool diag = p.causal && (kv0 + C::BN > tile * C::BM);
-            if (tail || diag) {
-                const int lim = p.causal ? min(len - 1, qpos) : (len - 1);  // last allowed key
+            if (kv0 + C::BN - 1 > lim) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (kv0 + c > lim) s[c] = -INFINITY;
@@ -319,98 +372,76 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                                    fmaxf(mxa[6], mxa[7]));
             const float m_new = fmaxf(m_ref, mx * sl2);
             const bool need = m_new > m_ref + 8.0f;
-            if (need && j == 0) {
+            if (j == 0) {
                 m_ref = m_new;
-            }
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
+            } else if (__any_sync(0xffffffffu, need)) {
+                // O_t holds P_{j-1} V_{j-1} complete: the commit that signalled S_j
+                // covers every MMA issued before it
                 const float alpha = need ? ex2(m_ref - m_new) : 1.0f;
                 if (need) {
                     l *= alpha;
                     lr *= alpha;
                     m_ref = m_new;
                 }
-                // O must hold PV_{j-1} before it is rescaled
-                const int pj = j - 1;
-                ok = mbar_wait(bar(BAR_PVDONE + (pj & 1)), (uint32_t)(pj >> 1) & 1u, p.status,
-                               abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t orr[32];
-                    tmem_ld32(tmem + lane_base + C::COL_O + c, orr);
+#pragma unroll 1
+                for (int c = 0; c < D; c += 16) {
+                    uint32_t orr[16];
+                    tmem_ld16(ocol + c, orr);
                     tc_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
+                    for (int e = 0; e < 16; ++e)
                         orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st16(tmem + lane_base + C::COL_O + c,
-                              *reinterpret_cast<uint32_t(*)[16]>(&orr[0]));
-                    tmem_st16(tmem + lane_base + C::COL_O + c + 16,
-                              *reinterpret_cast<uint32_t(*)[16]>(&orr[16]));
+                    tmem_st16(ocol + c, orr);
                 }
-                tc_wait_st();
             }
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            uint32_t pk[64];
             // P = 2^(s*scale*log2e - M); the exact row sum feeds the log-sum-exp, and the
             // row sum of the bf16-rounded P (the values the PV product uses) normalises O,
-            // so O / L stays an exact convex combination of V rows
-            float le[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            float lq[4] = {0.f, 0.f, 0.f, 0.f};
+            // so O / L stays an exact convex combination of V rows.  P goes over the first
+            // 64 columns of the S buffer it came from, 32 values (16 columns) at a time,
+            // so the S registers of a chunk are free once it is stored.
+            float le[4] = {0.f, 0.f, 0.f, 0.f};
+            float lq[2] = {0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 128; c += 2) {
-                float t0, t1;
-                ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_use, -m_use);
-                const float p0 = ex2(t0);
-                const float p1 = ex2(t1);
-                const uint32_t pp = pack_bf16(p0, p1);
-                const int a = (c >> 1) & 3;
-                fadd2(le[2 * a], le[2 * a + 1], p0, p1);
-                add_bf16x2_to(lq[a], pp);
-                pk[c >> 1] = pp;
-            }
-            l += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
-            lr += (lq[0] + lq[1]) + (lq[2] + lq[3]);
-            if (j >= 2) {
-                // P buffer sb was last read by PV_{j-2}
-                ok = mbar_wait(bar(BAR_PVDONE + sb), (uint32_t)((j - 2) >> 1) & 1u, p.status,
-                               abort_flag);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
+            for (int cb = 0; cb < 128; cb += 32) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = cb; c < cb + 32; c += 2) {
+                    float t0, t1;
+                    ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_use, -m_use);
+                    const float p0 = ex2(t0);
+                    const float p1 = ex2(t1);
+                    const uint32_t pp = pack_bf16(p0, p1);
+                    const int a = (c >> 1) & 1;
+                    fadd2(le[2 * a], le[2 * a + 1], p0, p1);
+                    add_bf16x2_to(lq[a], pp);
+                    pk[(c - cb) >> 1] = pp;
                 }
-                tc_fence_after();
+                tmem_st16(scol + (cb >> 1), pk);
             }
-            const uint32_t pcol = tmem + lane_base + (sb ? C::COL_P1 : C::COL_P0);
-            tmem_st16(pcol + 0, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-            tmem_st16(pcol + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-            tmem_st16(pcol + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
-            tmem_st16(pcol + 48, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
+            l += (le[0] + le[1]) + (le[2] + le[3]);
+            lr += lq[0] + lq[1];
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_PFULL + sb));
+            if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
         }
-        if (ok) {
+        if (ok && n_mine > 0) {
             // ---- epilogue: O / L -> bf16, LSE
-            const int last = n_kv - 1;
-            ok = mbar_wait(bar(BAR_PVDONE + (last & 1)), (uint32_t)(last >> 1) & 1u, p.status,
-                           abort_flag);
+            ok = mbar_wait(bar(BAR_OFULL + t), 0u, p.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
                 const bool row_ok = qpos < len;
                 const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
+                const int h = t ? head[1] : head[0];
                 const long long tok = (long long)tok0 + qpos;
                 __nv_bfloat16 *orow =
                     p.o + ((p.cu_seqlens ? tok : (long long)batch * p.N + qpos) * p.Hq + h) * D;
 #pragma unroll
                 for (int c = 0; c < D; c += 32) {
                     uint32_t orr[32];
-                    tmem_ld32(tmem + lane_base + C::COL_O + c, orr);
+                    tmem_ld32(ocol + c, orr);
                     tc_wait_ld();
                     uint32_t pkd[16];
 #pragma unroll
@@ -438,7 +469,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
