@@ -19,7 +19,7 @@ __all__ = [
     "AttnError", "load_library", "attn_fwd", "attn_fwd_f32", "attn_fwd_varlen",
     "attn_decode_paged", "attn_decode_paged_noalloc", "attn_decode_workspace_size",
     "attn_status_string",
-    "attn_get_device_status", "attn_version",
+    "attn_get_device_status", "attn_version", "attn_last_cuda_error",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +38,10 @@ _lib = None
 class AttnError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = int(code)
-        super().__init__("%s: %s (status %d)" % (where, attn_status_string(code), code))
+        msg = "%s: %s (status %d)" % (where, attn_status_string(code), code)
+        if self.code == ATTN_ERR_CUDA:
+            msg += " [%s]" % attn_last_cuda_error()
+        super().__init__(msg)
 
 
 def load_library(path: str = LIB_PATH):
@@ -63,6 +66,8 @@ def load_library(path: str = LIB_PATH):
         lib.attn_get_device_status.argtypes = [P]
         lib.attn_version.argtypes = []
         lib.attn_version.restype = ctypes.c_char_p
+        lib.attn_last_cuda_error.argtypes = []
+        lib.attn_last_cuda_error.restype = ctypes.c_char_p
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
                      "attn_decode_paged_noalloc", "attn_get_device_status"):
             getattr(lib, name).restype = ctypes.c_int
@@ -76,6 +81,11 @@ def attn_status_string(code: int) -> str:
 
 def attn_version() -> str:
     return load_library().attn_version().decode()
+
+
+def attn_last_cuda_error() -> str:
+    """Text of the last CUDA failure behind an ATTN_ERR_CUDA on this thread."""
+    return load_library().attn_last_cuda_error().decode()
 
 
 def _ptr(t):

@@ -9,6 +9,7 @@
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include "attn07.h"
@@ -35,10 +36,27 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// The last CUDA failure seen by an entry point on this host thread (reported by
+// attn_last_cuda_error).
+thread_local char g_last_cuda_error[160] = "no CUDA error recorded";
+
 attn_status_t cuda_fail(cudaError_t e) {
     (void)cudaGetLastError();
-    (void)e;
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e));
     return ATTN_ERR_CUDA;
+}
+
+attn_status_t driver_fail(CUresult r, const char *what) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s failed with CUresult %d", what,
+             (int)r);
+    return ATTN_ERR_CUDA;
+}
+
+// status of the launches just enqueued
+attn_status_t launch_status() {
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 // Per-device one-time set-up: SM count, status word address, kernel attributes.
@@ -93,7 +111,7 @@ attn_status_t make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64
                           const_cast<void *>(ptr), dims, strides_bytes, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+    return r == CUDA_SUCCESS ? ATTN_OK : driver_fail(r, "cuTensorMapEncodeTiled");
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -148,8 +166,7 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
         prefill_tc_kernel<64><<<(unsigned)grid, PrefillCfg<64>::THREADS, PrefillCfg<64>::SMEM,
                                 stream>>>(p, mq, mk, mv);
     }
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return launch_status();
 }
 
 }  // namespace
@@ -157,6 +174,8 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
 extern "C" {
 
 const char *attn_version(void) { return "attn07 0.1.0 sm_103a"; }
+
+const char *attn_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char *attn_status_string(attn_status_t s) {
     switch (s) {
@@ -248,8 +267,7 @@ attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float
     dim3 grid((N + kSimtBM - 1) / kSimtBM, Hq, B);
     prefill_simt_kernel<<<grid, kSimtThreads, prefill_simt_smem_bytes(d),
                           reinterpret_cast<cudaStream_t>(stream)>>>(p);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return launch_status();
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_per_seq,
@@ -324,11 +342,9 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
     const int G = st->sms;
     const size_t smem = dec_smem_bytes(Hkv, d, stages);
     decode_split_kernel<<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
+    if ((s = launch_status()) != ATTN_OK) return s;
     decode_merge_kernel<<<B, 256, 0, cs>>>(p, G);
-    e = cudaGetLastError();
-    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return launch_status();
 }
 
 // ---------------------------------------------------------------- no-allocation decode

@@ -188,6 +188,14 @@ attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_cache, cons
                                         int page_size, int num_pages, int max_pages_per_seq,
                                         float scale, attn_stream_t stream);
 
+/*
+ * Text of the last CUDA runtime or driver failure that made an entry point
+ * return ATTN_ERR_CUDA on the calling host thread (error name and message), or
+ * "no CUDA error recorded".  The pointer stays valid until the thread's next
+ * failing call; the text is not cleared by successful calls.
+ */
+const char *attn_last_cuda_error(void);
+
 /* Library version, e.g. "attn07 0.1.0 sm_103a". */
 const char *attn_version(void);
 

@@ -97,3 +97,16 @@ def test_binding_requires_library(tmp_path):
             mod.load_library(str(tmp_path / "missing.so"))
     finally:
         importlib.reload(A)
+
+
+def test_cuda_failure_text_is_recorded(lib):
+    # without a usable device, a valid call fails in the CUDA runtime: the status is
+    # ATTN_ERR_CUDA and the failure's name is kept for the caller's thread
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: this checks the failure path")
+    assert _fwd(lib) == A.ATTN_ERR_CUDA
+    text = A.attn_last_cuda_error()
+    assert text.startswith("cuda") and "no CUDA error recorded" not in text, text
+    with pytest.raises(A.AttnError, match=r"CUDA error \(status 3\) \[cuda"):
+        A._check(A.ATTN_ERR_CUDA, "attn_fwd")
