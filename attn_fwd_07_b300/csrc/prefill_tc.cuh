@@ -15,32 +15,28 @@
 // query heads of the same group on the same rows when the group size is even,
 // else two consecutive row tiles of one head.  Both tiles use every K_j and
 // V_j tile loaded into shared memory, which halves the load traffic per MMA,
-// and each tile's softmax runs while the tensor core works on the other tile
-// ("ping-pong").
+// and the two tiles' softmax runs while the tensor core works on the other
+// tile ("ping-pong").
 //
-// Warp roles (576 threads):
-//   warps 0-3, 8-11    softmax of tile 0; warps 4-7, 12-15  softmax of tile 1.
-//               Warp w serves TMEM lanes 32*(w%4) .. +31 (one query row per
-//               thread); warps below 8 take score columns 0-63 of their rows,
-//               warps 8-15 columns 64-127.  Warps w and w+8 hold the two halves
-//               of the same rows, run on the same SM sub-partition, and meet at
-//               a named barrier once per key tile to combine their row maxima.
-//   warp 16     TMA producer: both Q tiles once, then K_j / V_j (128 keys)
+// Warp roles (384 threads):
+//   warps 0-3   softmax of tile 0, one thread per query row (TMEM lane)
+//   warps 4-7   softmax of tile 1
+//   warp 8      TMA producer: both Q tiles once, then K_j / V_j (128 keys)
 //               into two shared-memory rings (128-byte swizzle)
-//   warp 17     MMA issuer (one thread), in this order for every j (PV with N = d
-//               in one instruction per 16 keys: N = 64 instructions run at about
-//               70% of the tensor core's rate, N = 128 at full rate):
+//   warp 9      MMA issuer (one thread), in this order for every j (PV with N = d
+//               in one instruction per 16 keys: M128 N64 instructions run at about
+//               70% of the tensor core's rate, N128 at full rate):
 //                  O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,
 //                  O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
 //               tcgen05.mma ops of one thread execute in issue order, so
 //               S_{j+1} never overwrites P_j before O += P_j V_j has read it,
 //               and a commit after S_{j+1} also covers that PV product.
+//   warps 10-11 idle (they complete the third warpgroup)
 //
-// Softmax step for tile t and key tile j (thread = row, one 64-column half):
-// load the half row of S from TMEM, mask (causal diagonal / sequence end),
-// half-row maximum, combine with the other half's through shared memory,
-// P = 2^(S * scale * log2e - M) rounded to bf16 and written back over the S
-// columns (P is the A operand of the PV product, read from TMEM), row sums.
+// Softmax step for tile t and key tile j (thread = row): load the S row from
+// TMEM, mask (causal diagonal / sequence end), running maximum, P = 2^(S *
+// scale * log2e - M) rounded to bf16 and written back over the S columns it
+// came from (P is the A operand of the PV product, read from TMEM), row sums.
 //
 // Rescaling: the row maximum used in the exponent only moves when the new
 // maximum exceeds it by more than 8 (log2 units).  Until then P may reach
@@ -80,25 +76,17 @@ struct PrefillCfg {
     static constexpr int NH = D / 64;                     // 64-column halves of a row
     static constexpr uint32_t HALF = 128u * 128u;         // one [128 rows][64] bf16 half: 16 KB
     static constexpr uint32_t TILE = NH * HALF;
-    static constexpr int SK = (D == 128) ? 2 : 4;         // K ring stages
+    static constexpr int SK = (D == 128) ? 3 : 4;         // K ring stages
     static constexpr int SV = (D == 128) ? 2 : 4;         // V ring stages
     static constexpr uint32_t OFF_Q = 0;                  // Q_0, Q_1
     static constexpr uint32_t OFF_K = 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + SK * TILE;
     static constexpr uint32_t OFF_CTRL = OFF_V + SV * TILE;
-    // control block: barriers and the TMEM address (256 B), then the exchange
-    // between the two halves of a row: [tile][half][row] maxima, sums of P and of the
-    // rounded P (3 x 2 KB), and [tile][half][row quarter] status flags
-    static constexpr uint32_t OFF_XMAX = 256;
-    static constexpr uint32_t OFF_XL = OFF_XMAX + 2048;
-    static constexpr uint32_t OFF_XLR = OFF_XL + 2048;
-    static constexpr uint32_t OFF_XOK = OFF_XLR + 2048;
-    static constexpr uint32_t CTRL_BYTES = OFF_XOK + 64;
+    static constexpr uint32_t CTRL_BYTES = 512;
     static constexpr size_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
     // TMEM columns
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
-    static constexpr int THREADS = 576;
-    static constexpr int WARP_TMA = 16, WARP_MMA = 17;
+    static constexpr int THREADS = 384;
 };
 
 // barrier slots inside the control block (8 bytes each)
@@ -116,7 +104,7 @@ enum : uint32_t {
 };
 
 template <int D>
-__global__ void __launch_bounds__(576, 1)
+__global__ void __launch_bounds__(384, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using C = PrefillCfg<D>;
@@ -173,7 +161,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (warp == C::WARP_TMA && lane == 0) {
+    if (threadIdx.x == 256) {
         mbar_init(bar(BAR_Q), 1);
         for (int s = 0; s < C::SK; ++s) {
             mbar_init(bar(BAR_KFULL + s), 1);
@@ -185,14 +173,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(BAR_SFULL + t), 1);
-            mbar_init(bar(BAR_PFULL + t), 8);
+            mbar_init(bar(BAR_PFULL + t), 4);
             mbar_init(bar(BAR_OFULL + t), 1);
         }
         mbar_init(bar(BAR_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == C::WARP_MMA) {
+    if (warp == 9) {
         tmem_alloc(ctrl + 8 * BAR_COUNT, 512);
         tmem_relinquish();
     }
@@ -201,7 +189,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == C::WARP_TMA) {
+    if (warp == 8) {
         // ============================ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmQ);
@@ -253,12 +241,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 mbar_wait(bar(BAR_Q), 0u, p.status, nullptr);
             }
         }
-    } else if (warp == C::WARP_MMA) {
+    } else if (warp == 9) {
         // ============================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
-            // PV: N = d in one instruction per 16 keys; V is MN-major, its two 64-dim
-            // halves (128-byte swizzle atoms) 16 KB apart (the descriptor's leading offset)
+            // PV: V is MN-major; its two 64-dim halves (128-byte swizzle atoms) lie 16 KB
+            // apart, which the descriptor's leading offset describes
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
             // S_t = Q_t K_j^T into S buffer t
             auto issue_qk = [&](int t, int j) {
@@ -334,72 +322,54 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             tc_commit(bar(BAR_DRAIN));
             mbar_wait(bar(BAR_DRAIN), 0u, p.status, nullptr);
         }
-    } else {
-        // ============================ softmax: tile t, columns [64 h, 64 h + 64)
-        const int t = (warp >> 2) & 1;
-        const int hh = warp >> 3;                  // half of the row
-        const int q4 = warp & 3;                   // lane quarter = 32-row group
+    } else if (warp < 8) {
+        // ============================ softmax: warpgroup t, thread = query row
+        const int t = warp >> 2;
         const int n_mine = t ? nt[1] : nt[0];
-        const int r = q4 * 32 + lane;              // row in tile = TMEM lane
-        const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+        const int r = threadIdx.x & 127;           // row in tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t scol = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
-        const uint32_t ocol = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0) + hh * (D / 2);
+        const uint32_t ocol = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
         const int qpos = (t ? row0[1] : row0[0]) + r;  // position within the sequence
         const int lim = p.causal ? min(len - 1, qpos) : (len - 1);  // last allowed key
-        // exchange slots: mine [t][hh][r], the other half's [t][1-hh][r]
-        float *xmax = reinterpret_cast<float *>(ctrl_ptr + C::OFF_XMAX);
-        float *xl = reinterpret_cast<float *>(ctrl_ptr + C::OFF_XL);
-        float *xlr = reinterpret_cast<float *>(ctrl_ptr + C::OFF_XLR);
-        volatile int *xok = reinterpret_cast<volatile int *>(ctrl_ptr + C::OFF_XOK);
-        const int mine = (t * 2 + hh) * 128 + r, other = (t * 2 + (hh ^ 1)) * 128 + r;
-        const int okmine = (t * 2 + hh) * 4 + q4, okother = (t * 2 + (hh ^ 1)) * 4 + q4;
-        const uint32_t pair_bar = 1u + (uint32_t)(t * 4 + q4);  // named barrier of the pair
         float m_ref = -INFINITY;                   // log2 units, scaled
-        float l = 0.f;                             // sum of P over my half (fp32) -> LSE
+        float l = 0.f;                             // sum of P (fp32) -> LSE
         float lr = 0.f;                            // sum of bf16-rounded P -> normalises O
         const float sl2 = p.scale_log2;
         bool ok = true;
         for (int j = 0; j < n_mine; ++j) {
             ok = mbar_wait(bar(BAR_SFULL + t), (uint32_t)j & 1u, p.status, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            uint32_t sr[64];
-            float *s = reinterpret_cast<float *>(sr);
-            float pmax = -INFINITY;
-            if (ok) {
-                tc_fence_after();
-                tmem_ld32(scol + hh * 64 + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(scol + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                tc_wait_ld();
-                const int kv0 = j * C::BN + hh * 64;
-                if (kv0 + 63 > lim) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (kv0 + c > lim) s[c] = -INFINITY;
-                }
-                // half-row maximum: eight independent 3-input max chains
-                float mxa[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = fmax3(s[i], s[i + 8], s[i + 16]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[24 + i], s[32 + i]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[40 + i], s[48 + i]);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(mxa[i], s[56 + i]);
-                pmax = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
-                             fmaxf(mxa[6], mxa[7]));
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
             }
-            // combine with the other half: both halves take the same decision to go on
-            // (so neither waits at the barrier for a partner that left), and after the
-            // barrier the other half's S loads are complete, so P may overwrite them
-            xmax[mine] = pmax;
-            if (lane == 0) xok[okmine] = ok ? 1 : 0;
-            tc_fence_before();
-            named_bar_sync(pair_bar, 64);
             tc_fence_after();
-            ok = ok && xok[okother] != 0;
-            if (!ok) break;
-            const float mx = fmaxf(pmax, xmax[other]);
+            uint32_t sr[128];
+            tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+            tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+            tc_wait_ld();
+
+            float *s = reinterpret_cast<float *>(sr);
+            const int kv0 = j * C::BN;
+            if (kv0 + C::BN - 1 > lim) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (kv0 + c > lim) s[c] = -INFINITY;
+            }
+            // row maximum: eight independent 3-input max chains
+            float mxa[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mxa[i] = fmax3(s[i], s[i + 8], s[i + 16]);
+#pragma unroll
+            for (int c = 24; c + 16 <= 120; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(mxa[i], s[120 + i]);
+            const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+                                   fmaxf(mxa[6], mxa[7]));
             const float m_new = fmaxf(m_ref, mx * sl2);
             const bool need = m_new > m_ref + 8.0f;
             if (j == 0) {
@@ -414,7 +384,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     m_ref = m_new;
                 }
 #pragma unroll 1
-                for (int c = 0; c < D / 2; c += 16) {
+                for (int c = 0; c < D; c += 16) {
                     uint32_t orr[16];
                     tmem_ld16(ocol + c, orr);
                     tc_wait_ld();
@@ -427,16 +397,16 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
             // P = 2^(s*scale*log2e - M); the exact row sum feeds the log-sum-exp, and the
             // row sum of the bf16-rounded P (the values the PV product uses) normalises O,
-            // so O / L stays an exact convex combination of V rows.  My 64 values of P go
-            // to P columns [32 hh, 32 hh + 32) (S columns of the first half), 16 values
-            // (8 columns) at a time.
+            // so O / L stays an exact convex combination of V rows.  P goes over the first
+            // 64 columns of the S buffer it came from, 32 values (16 columns) at a time,
+            // so the S registers of a chunk are free once it is stored.
             float le[4] = {0.f, 0.f, 0.f, 0.f};
             float lq[2] = {0.f, 0.f};
 #pragma unroll
-            for (int cb = 0; cb < 64; cb += 16) {
-                uint32_t pk[8];
+            for (int cb = 0; cb < 128; cb += 32) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = cb; c < cb + 16; c += 2) {
+                for (int c = cb; c < cb + 32; c += 2) {
                     float t0, t1;
                     ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_use, -m_use);
                     const float p0 = ex2(t0);
@@ -447,7 +417,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     add_bf16x2_to(lq[a], pp);
                     pk[(c - cb) >> 1] = pp;
                 }
-                tmem_st8(scol + hh * 32 + (cb >> 1), pk);
+                tmem_st16(scol + (cb >> 1), pk);
             }
             l += (le[0] + le[1]) + (le[2] + le[3]);
             lr += lq[0] + lq[1];
@@ -457,25 +427,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
         }
         if (ok && n_mine > 0) {
-            // ---- epilogue: row sums of both halves, then my half of O / L -> bf16, LSE
-            xl[mine] = l;
-            xlr[mine] = lr;
-            named_bar_sync(pair_bar, 64);
-            const float lt = l + xl[other];
-            const float lrt = lr + xlr[other];
+            // ---- epilogue: O / L -> bf16, LSE
             ok = mbar_wait(bar(BAR_OFULL + t), 0u, p.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
                 const bool row_ok = qpos < len;
-                const float inv = (lrt > 0.f) ? 1.f / lrt : 0.f;
+                const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
                 const int h = t ? head[1] : head[0];
                 const long long tok = (long long)tok0 + qpos;
                 __nv_bfloat16 *orow =
-                    p.o + ((p.cu_seqlens ? tok : (long long)batch * p.N + qpos) * p.Hq + h) * D +
-                    hh * (D / 2);
+                    p.o + ((p.cu_seqlens ? tok : (long long)batch * p.N + qpos) * p.Hq + h) * D;
 #pragma unroll
-                for (int c = 0; c < D / 2; c += 32) {
+                for (int c = 0; c < D; c += 32) {
                     uint32_t orr[32];
                     tmem_ld32(ocol + c, orr);
                     tc_wait_ld();
@@ -492,8 +456,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                                                 pkd[4 * e + 3]);
                     }
                 }
-                if (row_ok && p.lse && hh == 0) {
-                    const float lse = (lt > 0.f) ? (m_ref + __log2f(lt)) * kLn2 : -INFINITY;
+                if (row_ok && p.lse) {
+                    const float lse = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
                     const long long idx = p.cu_seqlens ? (long long)h * p.total + tok
                                                        : ((long long)batch * p.Hq + h) * p.N + qpos;
                     p.lse[idx] = lse;
@@ -505,7 +469,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == C::WARP_MMA) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
