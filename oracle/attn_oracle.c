@@ -198,6 +198,59 @@ int oracle_attn_fwd(const float *q, const float *k, const float *v,
 }
 
 /*
+ * Local ("sliding window") attention, yapayzekasozluk.tr "attention" tag
+ * page, entry "Sliding Window Attention": each token attends only to the
+ * tokens within a window around its own position instead of the whole
+ * sequence (the page's form: w/2 to the left and w/2 to the right).  Written
+ * with separate left and right extents: query i of a sequence of n tokens
+ * sees keys j with
+ *       i - wl <= j <= i + wr     and 0 <= j < n,
+ * where wl < 0 (or wr < 0) means no limit on that side; wl < 0, wr = 0 is
+ * causal attention and wl < 0, wr < 0 is full attention.  Same layouts and
+ * row list as oracle_attn_rows (queries and keys of the same length N).
+ */
+int oracle_attn_window_rows(const float *q, const float *k, const float *v,
+                            int B, int Hq, int Hkv, int N, int d, int wl, int wr,
+                            double scale, const int32_t *rows, int64_t nrows,
+                            double *o_rows, double *lse_rows, int nthreads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || N < 0 || d <= 0) return -1;
+    const int group = Hq / Hkv;
+    const int nt = set_threads(nthreads);
+    int bad = 0;
+#pragma omp parallel num_threads(nt) reduction(| : bad)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        const float **kr = (const float **)malloc(sizeof(float *) * (size_t)(N > 0 ? N : 1));
+        const float **vr = (const float **)malloc(sizeof(float *) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+            if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= N) {
+                bad = 1;
+                continue;
+            }
+            const int g = h / group;
+            /* the allowed keys form one contiguous range [lo, hi] */
+            int64_t lo = 0, hi = (int64_t)N - 1;
+            if (wl >= 0 && (int64_t)i - wl > lo) lo = (int64_t)i - wl;
+            if (wr >= 0 && (int64_t)i + wr < hi) hi = (int64_t)i + wr;
+            const int64_t n = hi >= lo ? hi - lo + 1 : 0;
+            for (int64_t j = 0; j < n; ++j) {
+                kr[j] = k + (((int64_t)b * N + lo + j) * Hkv + g) * d;
+                vr[j] = v + (((int64_t)b * N + lo + j) * Hkv + g) * d;
+            }
+            const float *qr = q + (((int64_t)b * N + i) * Hq + h) * d;
+            attention_row(qr, kr, vr, n, d, scale, s, o_rows + r * d, lse_rows + r);
+        }
+        free(s);
+        free(kr);
+        free(vr);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
  * Variable-length packed attention.  Sequence s owns tokens
  * cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed arrays; each sequence is
  * its own independent attention problem (its queries see only its keys).

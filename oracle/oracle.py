@@ -49,6 +49,8 @@ def _load():
         D = ctypes.c_double
         lib.oracle_attn_rows.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P, I64, P, P, I]
         lib.oracle_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, D, I]
+        lib.oracle_attn_window_rows.argtypes = [P, P, P, I, I, I, I, I, I, I, D, P, I64, P, P,
+                                                I]
         lib.oracle_attn_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D, I]
         lib.oracle_decode_paged_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D,
                                                  P, I, P, P, I]
@@ -58,6 +60,7 @@ def _load():
         lib.oracle_merge_parts.restype = None
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_attn_varlen",
+                     "oracle_attn_window_rows",
                      "oracle_decode_paged_rows", "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -114,6 +117,37 @@ def attn_rows(q, k, v, rows, causal: bool, scale: float, nthreads: int = 0):
     if rc != 0:
         raise ValueError("oracle_attn_rows rejected its arguments")
     return o, lse
+
+
+def attn_window_rows(q, k, v, rows, window_left: int, window_right: int, scale: float,
+                     nthreads: int = 0):
+    """Sliding-window attention for selected rows (b, h, i): query i sees keys
+    i - window_left .. i + window_right (a negative extent: no limit on that side).
+    q [B,N,Hq,d], k/v [B,N,Hkv,d] -> (o [n, d], lse [n])."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, N, Hkv, d) and v.shape == k.shape
+    rows = _i32(rows).reshape(-1, 3)
+    n = rows.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_attn_window_rows(_p(q), _p(k), _p(v), B, Hq, Hkv, N, d,
+                                         int(window_left), int(window_right), float(scale),
+                                         _p(rows), n, _p(o), _p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_window_rows rejected its arguments")
+    return o, lse
+
+
+def attn_window(q, k, v, window_left: int, window_right: int, scale: float,
+                nthreads: int = 0):
+    """Sliding-window attention for every row -> (o [B,N,Hq,d], lse [B,Hq,N])."""
+    B, N, Hq, d = np.shape(q)
+    b, h, i = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(N), indexing="ij")
+    rows = np.stack([b.ravel(), h.ravel(), i.ravel()], 1)
+    o, lse = attn_window_rows(q, k, v, rows, window_left, window_right, scale, nthreads)
+    return (o.reshape(B, Hq, N, d).transpose(0, 2, 1, 3).copy(), lse.reshape(B, Hq, N))
 
 
 def attn_varlen(q, k, v, cu_seqlens, causal: bool, scale: float, nthreads: int = 0):
