@@ -16,7 +16,7 @@ import os
 import torch
 
 __all__ = [
-    "AttnError", "load_library", "attn_fwd", "attn_fwd_f32", "attn_fwd_varlen",
+    "AttnError", "load_library", "attn_fwd", "attn_fwd_window", "attn_fwd_f32", "attn_fwd_varlen",
     "attn_decode_paged", "attn_decode_paged_noalloc", "attn_decode_workspace_size",
     "attn_status_string",
     "attn_get_device_status", "attn_version", "attn_last_cuda_error",
@@ -55,6 +55,7 @@ def load_library(path: str = LIB_PATH):
         P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]
         lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
@@ -69,6 +70,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_last_cuda_error.argtypes = []
         lib.attn_last_cuda_error.restype = ctypes.c_char_p
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
+                     "attn_fwd_window",
                      "attn_decode_paged_noalloc", "attn_get_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -126,6 +128,29 @@ def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, o=None, l
     rc = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N,
                                  d, int(bool(causal)), float(scale), _stream(stream))
     _check(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_window(q, k, v, window_left: int, window_right: int, scale: float | None = None,
+                    o=None, lse=None, want_lse: bool = True, stream=None):
+    """bf16 sliding-window prefill: query i sees keys i - window_left .. i + window_right
+    (-1: unbounded side).  Layouts as attn_fwd."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [B, N, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq,
+                                        Hkv, N, d, int(window_left), int(window_right),
+                                        float(scale), _stream(stream))
+    _check(rc, "attn_fwd_window")
     return o, lse
 
 

@@ -120,8 +120,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // `nbatch` sequences along the outermost axis (dense) or one packed axis (varlen).
 attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, void *o, float *lse,
                                 const int32_t *cu_seqlens, int nseq, int N_or_total,
-                                int ntiles, int Hq, int Hkv, int d, int causal, float scale,
-                                cudaStream_t stream) {
+                                int ntiles, int Hq, int Hkv, int d, int wl, int wr,
+                                float scale, cudaStream_t stream) {
     DeviceState *st = nullptr;
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
@@ -153,7 +153,8 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     // a CTA takes two query heads of one group on the same rows when the group size is
     // even, else two consecutive row tiles of one head
     p.head_pairs = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
-    p.causal = causal ? 1 : 0;
+    p.wl = wl < 0 ? -1 : wl;
+    p.wr = wr < 0 ? -1 : wr;
     p.scale_log2 = scale * kLog2e;
     const long long grid = p.head_pairs ? (long long)ntiles * (Hq / 2) * nseq
                                         : (long long)((ntiles + 1) / 2) * Hq * nseq;
@@ -217,8 +218,23 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
     if ((long long)B * N * Hq * d > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
     const int ntiles = (N + 127) / 128;
-    return launch_prefill_tc(q, k, v, o, lse, nullptr, B, N, ntiles, Hq, Hkv, d, causal, scale,
-                             reinterpret_cast<cudaStream_t>(stream));
+    return launch_prefill_tc(q, k, v, o, lse, nullptr, B, N, ntiles, Hq, Hkv, d, -1,
+                             causal ? 0 : -1, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int Hq, int Hkv, int N, int d, int window_left,
+                              int window_right, float scale, attn_stream_t stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)B * N * Hq * d > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
+    const int ntiles = (N + 127) / 128;
+    return launch_prefill_tc(q, k, v, o, lse, nullptr, B, N, ntiles, Hq, Hkv, d, window_left,
+                             window_right, scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -235,7 +251,7 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     if (total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
     const int ntiles = (max_seqlen + 127) / 128;
     return launch_prefill_tc(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, ntiles, Hq, Hkv,
-                             d, causal, scale, reinterpret_cast<cudaStream_t>(stream));
+                             d, -1, causal ? 0 : -1, scale, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,

@@ -65,7 +65,8 @@ struct PrefillParams {
     int Hq, Hkv;
     int ntiles;     // 128-row query tiles per sequence (of the longest sequence)
     int head_pairs; // 1: a CTA takes two heads of a group on the same rows; 0: two row tiles
-    int causal;
+    int wl, wr;     // query i sees keys i - wl .. i + wr; -1: no limit on that side
+                    // (causal: wl = -1, wr = 0; full: wl = wr = -1)
     float scale_log2;
 };
 
@@ -129,8 +130,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         len = p.N;
         batch = sq;
     }
-    // the CTA's two tiles: query head and first row of each
-    int head[2], row0[2], nt[2];
+    // the CTA's two tiles: query head, first row, and the key tiles [jlo, jhi] each needs
+    int head[2], row0[2], jlo[2], jhi[2];
     if (p.head_pairs) {
         head[0] = 2 * hu;
         head[1] = 2 * hu + 1;
@@ -141,13 +142,27 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         row0[1] = row0[0] + C::BM;
     }
     const int g = head[0] / (p.Hq / p.Hkv);
-    const int nkv_all = (len + C::BN - 1) / C::BN;
+    bool valid[2];
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
-        nt[t] = (outer < 0 || row0[t] >= len) ? 0
-                : (p.causal ? min(row0[t] / C::BN + 1, nkv_all) : nkv_all);
-    if (nt[0] == 0 && nt[1] == 0) return;  // uniform: nothing to do
-    const int n_kv = max(nt[0], nt[1]);
+    for (int t = 0; t < 2; ++t) {
+        valid[t] = outer >= 0 && row0[t] < len;
+        const int last_row = min(row0[t] + C::BM, len) - 1;
+        const int lo_key = p.wl < 0 ? 0 : max(0, row0[t] - p.wl);
+        const int hi_key = p.wr < 0 ? len - 1 : min(len - 1, last_row + p.wr);
+        jlo[t] = lo_key / C::BN;
+        jhi[t] = hi_key / C::BN;
+    }
+    if (!valid[0] && !valid[1]) return;  // uniform: nothing to do
+    // key tiles J0 .. J0 + n_kv - 1 cover both tiles; ring slots count from J0
+    const int J0 = valid[0] ? (valid[1] ? min(jlo[0], jlo[1]) : jlo[0]) : jlo[1];
+    const int J1 = valid[0] ? (valid[1] ? max(jhi[0], jhi[1]) : jhi[0]) : jhi[1];
+    const int n_kv = J1 - J0 + 1;
+    // tile t takes part in key tile J0 + i
+    auto uses = [&](int t, int i) {
+        const int j = J0 + i;
+        return (t ? valid[1] : valid[0]) && j >= (t ? jlo[1] : jlo[0]) &&
+               j <= (t ? jhi[1] : jhi[0]);
+    };
 
     const uint32_t raw = smem_u32(pf_smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -197,10 +212,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             prefetch_tmap(&tmV);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            mbar_arrive_expect_tx(bar(BAR_Q), (uint32_t)((nt[0] > 0) + (nt[1] > 0)) * C::TILE);
+            mbar_arrive_expect_tx(bar(BAR_Q), (uint32_t)(valid[0] + valid[1]) * C::TILE);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (nt[t] == 0) continue;
+                if (!valid[t]) continue;
 #pragma unroll
                 for (int hf = 0; hf < C::NH; ++hf)
                     tma_load_4d(base + C::OFF_Q + t * C::TILE + hf * C::HALF, &tmQ, bar(BAR_Q),
@@ -208,7 +223,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             }
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < n_kv; ++j) {
-                const int kvrow = tok0 + j * C::BN;
+                const int kvrow = tok0 + (J0 + j) * C::BN;
                 const int sk = j % C::SK;
                 if (!mbar_wait(bar(BAR_KEMPTY + sk), ((uint32_t)(j / C::SK) & 1u) ^ 1u, p.status,
                                abort_flag))
@@ -267,7 +282,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 tc_fence_after();
 #pragma unroll
                 for (int t = 0; t < 2; ++t)
-                    if (nt[t] > 0) issue_qk(t, 0);
+                    if (uses(t, 0)) issue_qk(t, 0);
                 tc_commit(bar(BAR_KEMPTY + 0));
             }
             for (int j = 0; ok && j < n_kv; ++j) {
@@ -276,30 +291,34 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 bool v_ready = false, k_ready = false;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
-                    if (j >= nt[t]) continue;
-                    if (!mbar_wait(bar(BAR_PFULL + t), (uint32_t)j & 1u, p.status, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    if (!v_ready) {
-                        if (!mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u, p.status,
-                                       abort_flag)) {
+                    // ring index j counts from J0; tile t's own count from its first key tile
+                    const int it = J0 + j - (t ? jlo[1] : jlo[0]);
+                    if (uses(t, j)) {
+                        if (!mbar_wait(bar(BAR_PFULL + t), (uint32_t)it & 1u, p.status, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        v_ready = true;
+                        if (!v_ready) {
+                            if (!mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u, p.status,
+                                           abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            v_ready = true;
+                        }
+                        tc_fence_after();
+                        // O_t += P_t V_j: P_t (bf16, 128 x 128) from the S_t columns of TMEM
+                        const uint32_t vb = base + C::OFF_V + sv * C::TILE;
+                        const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
+                        const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
+    #pragma unroll
+                        for (int kk = 0; kk < C::BN / 16; ++kk)
+                            tc_mma_ts(ocol, pcol + kk * 8,
+                                      smem_desc_sw128(vb + kk * 2048u, C::HALF, 1024), idesc_pv,
+                                      (it > 0 || kk > 0) ? 1u : 0u);
+                        if (!uses(t, j + 1)) tc_commit(bar(BAR_OFULL + t));
                     }
-                    tc_fence_after();
-                    // O_t += P_t V_j: P_t (bf16, 128 x 128) from the S_t columns of TMEM
-                    const uint32_t vb = base + C::OFF_V + sv * C::TILE;
-                    const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
-                    const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
-#pragma unroll
-                    for (int kk = 0; kk < C::BN / 16; ++kk)
-                        tc_mma_ts(ocol, pcol + kk * 8,
-                                  smem_desc_sw128(vb + kk * 2048u, C::HALF, 1024), idesc_pv,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
-                    if (j + 1 < nt[t]) {
+                    if (uses(t, j + 1)) {
                         if (!k_ready) {
                             if (!mbar_wait(bar(BAR_KFULL + sk1), (uint32_t)((j + 1) / C::SK) & 1u,
                                            p.status, abort_flag)) {
@@ -310,8 +329,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                             tc_fence_after();
                         }
                         issue_qk(t, j + 1);
-                    } else {
-                        tc_commit(bar(BAR_OFULL + t));
                     }
                 }
                 if (!ok) break;
@@ -325,13 +342,16 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     } else if (warp < 8) {
         // ============================ softmax: warpgroup t, thread = query row
         const int t = warp >> 2;
-        const int n_mine = t ? nt[1] : nt[0];
+        const int j_first = t ? jlo[1] : jlo[0];
+        const int n_mine = (t ? valid[1] : valid[0]) ? (t ? jhi[1] : jhi[0]) - j_first + 1 : 0;
         const int r = threadIdx.x & 127;           // row in tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t scol = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t ocol = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
         const int qpos = (t ? row0[1] : row0[0]) + r;  // position within the sequence
-        const int lim = p.causal ? min(len - 1, qpos) : (len - 1);  // last allowed key
+        // allowed keys of this row: [klo, khi]
+        const int klo = p.wl < 0 ? 0 : qpos - p.wl;
+        const int khi = p.wr < 0 ? len - 1 : min(len - 1, qpos + p.wr);
         float m_ref = -INFINITY;                   // log2 units, scaled
         float l = 0.f;                             // sum of P (fp32) -> LSE
         float lr = 0.f;                            // sum of bf16-rounded P -> normalises O
@@ -352,11 +372,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             tc_wait_ld();
 
             float *s = reinterpret_cast<float *>(sr);
-            const int kv0 = j * C::BN;
-            if (kv0 + C::BN - 1 > lim) {
+            const int kv0 = (j_first + j) * C::BN;
+            if (kv0 < klo || kv0 + C::BN - 1 > khi) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (kv0 + c > lim) s[c] = -INFINITY;
+                    if (kv0 + c < klo || kv0 + c > khi) s[c] = -INFINITY;
             }
             // row maximum: eight independent 3-input max chains
             float mxa[8];

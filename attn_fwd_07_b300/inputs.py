@@ -95,6 +95,7 @@ class Dense:
     v: torch.Tensor
     causal: bool
     scale: float
+    window: tuple | None = None   # (left, right) extents of a sliding window, -1 = unbounded
 
     @property
     def shape(self):
@@ -184,7 +185,7 @@ class Workload:
     description: str = ""
 
 
-# The five workloads: index = seed.
+# The workloads: seed = index (the five listed first, then the sliding-window one).
 WORKLOADS = {
     "single_head_f32": Workload(
         "single_head_f32", "dense", 1,
@@ -203,6 +204,14 @@ WORKLOADS = {
         dict(S=8, lo=512, hi=8192, Hq=32, Hkv=8, d=128, dtype=torch.bfloat16, factor=1.0,
              causal=True),
         "8 packed sequences, lengths U[512,8192], Hq=32 Hkv=8 d=128, bf16 N(0,1), causal"),
+    # local attention as the sliding-window glossary entry describes it: w/2 keys on
+    # either side of each token, here w = 4096 on an 8192-token sequence (the length
+    # the entry uses to count full attention's ~67 million pairs)
+    "swa_n8192_w4096": Workload(
+        "swa_n8192_w4096", "window", 6,
+        dict(B=1, N=8192, Hq=32, Hkv=8, d=128, dtype=torch.bfloat16, factor=1.0,
+             window=(2048, 2048)),
+        "B=1 Hq=32 Hkv=8 N=8192 d=128, bf16 N(0,1), sliding window of 2048 keys left and right"),
     "decode_paged_b64": Workload(
         "decode_paged_b64", "decode", 5,
         dict(B=64, lo=1024, hi=32768, Hq=32, Hkv=8, d=128, page_size=16,
@@ -223,6 +232,12 @@ def make(name: str, batch: int | None = None):
         B = p["B"] if batch is None else int(batch)
         return dense(B, p["N"], p["Hq"], p["Hkv"], p["d"], w.seed, p["dtype"], p["factor"],
                      p["causal"])
+    if w.kind == "window":
+        B = p["B"] if batch is None else int(batch)
+        out = dense(B, p["N"], p["Hq"], p["Hkv"], p["d"], w.seed, p["dtype"], p["factor"],
+                    causal=False)
+        out.window = tuple(p["window"])
+        return out
     if w.kind == "varlen":
         S = p["S"] if batch is None else int(batch)
         lens = lengths(S, p["lo"], p["hi"], w.seed)

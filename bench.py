@@ -201,7 +201,16 @@ def profiled_traffic(kernel: str, workload: str):
 
 def prefill_flops(w) -> float:
     """Algorithmic FLOPs of one prefill: 4*d per (query, key) pair (QK^T and PV, 2*d
-    each) over N^2 pairs per sequence and head, halved when causal (2*B*Hq*N^2*d)."""
+    each) over N^2 pairs per sequence and head, halved when causal (2*B*Hq*N^2*d); a
+    sliding window counts its allowed pairs exactly."""
+    if getattr(w, "window", None) is not None:
+        # a sliding window: the exact number of allowed (query, key) pairs
+        B, N, Hq, d = w.q.shape
+        wl, wr = w.window
+        i = np.arange(N, dtype=np.float64)
+        lo = np.zeros(N) if wl < 0 else np.maximum(0.0, i - wl)
+        hi = np.full(N, N - 1.0) if wr < 0 else np.minimum(N - 1.0, i + wr)
+        return 4.0 * Hq * d * B * float((hi - lo + 1).sum())
     if w.q.dim() == 4:
         B, N, Hq, d = w.q.shape
         pairs = B * float(N) * N
@@ -258,7 +267,12 @@ class Leg:
             self.dev = [t.to(dev) for t in self.host]
             q = self.dev[0]
             self.o = torch.empty_like(q)
-            if self.kind == "varlen":
+            if self.kind == "window":
+                B, N, Hq, d = w.q.shape
+                self.lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+                self.shape = {"B": B, "N": N, "Hq": Hq, "Hkv": int(w.k.shape[2]), "d": d,
+                              "window": list(w.window)}
+            elif self.kind == "varlen":
                 T, Hq, d = w.q.shape
                 self.max_len = int(w.lens.max())
                 self.lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
@@ -282,6 +296,9 @@ class Leg:
         if self.kind == "decode":
             A.attn_decode_paged(d[0], d[1], d[2], d[3], d[4], self.scale, o=self.o, lse=self.lse,
                                 workspace=self.ws, stream=stream)
+        elif self.kind == "window":
+            A.attn_fwd_window(d[0], d[1], d[2], self.w.window[0], self.w.window[1], self.scale,
+                              o=self.o, lse=self.lse, stream=stream)
         elif self.kind == "varlen":
             A.attn_fwd_varlen(d[0], d[1], d[2], d[3], self.max_len, self.w.causal, self.scale,
                               o=self.o, lse=self.lse, stream=stream)
@@ -353,8 +370,17 @@ def cpu_oracle_sample(w, kind: str, seconds: float, seed: int = 0):
         B, N, Hq, d = q.shape
         rows = np.stack([rng.integers(0, B, n_rows), rng.integers(0, Hq, n_rows),
                          rng.integers(0, N, n_rows)], 1).astype(np.int32)
-        oracle.attn_rows(q, k, v, rows, w.causal, w.scale)
-        keys = (rows[:, 2].astype(np.float64) + 1.0) if w.causal else np.full(n_rows, float(N))
+        win = getattr(w, "window", None)
+        if win is not None:
+            oracle.attn_window_rows(q, k, v, rows, win[0], win[1], w.scale)
+            i = rows[:, 2].astype(np.float64)
+            lo = np.zeros(n_rows) if win[0] < 0 else np.maximum(0.0, i - win[0])
+            hi = np.full(n_rows, N - 1.0) if win[1] < 0 else np.minimum(N - 1.0, i + win[1])
+            keys = hi - lo + 1
+        else:
+            oracle.attn_rows(q, k, v, rows, w.causal, w.scale)
+            keys = (rows[:, 2].astype(np.float64) + 1.0) if w.causal else np.full(n_rows,
+                                                                                 float(N))
         work += float(4.0 * keys.sum() * d)
         done += n_rows
         el = time.perf_counter() - t0

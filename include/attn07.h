@@ -83,6 +83,22 @@ attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, flo
                        attn_stream_t stream);
 
 /*
+ * attn_fwd_window -- attn_fwd with local ("sliding window") attention: query i
+ * of a sequence sees only keys j with  i - window_left <= j <= i + window_right
+ * (yapayzekasozluk.tr "attention" tag page, entry "Sliding Window Attention":
+ * each token attends to the tokens within a window around its own position,
+ * w/2 on either side in the page's form, so the work grows as N * w instead of
+ * N^2).  window_left / window_right >= 0 bound that side; -1 leaves it
+ * unbounded: (-1, 0) is causal attention, (-1, -1) full attention, (w/2, w/2)
+ * the page's symmetric window.  Every row sees at least its own key.  Key tiles
+ * wholly outside a row block's window are skipped.  Layouts, sizes and errors
+ * as attn_fwd; window values below -1 return ATTN_ERR_INVALID_ARG.
+ */
+attn_status_t attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int Hq, int Hkv, int N, int d, int window_left,
+                              int window_right, float scale, attn_stream_t stream);
+
+/*
  * attn_fwd_f32 -- the same operation with fp32 q, k, v and o (same layouts and
  * rules as attn_fwd).  Arithmetic is fp32 throughout (no reduced-precision
  * tensor-core path).  1 <= d <= 128 and d % 4 == 0.
