@@ -366,6 +366,67 @@ int oracle_decode_paged_rows(const float *q, const float *k_cache, const float *
 }
 
 /*
+ * Decode with a sliding window (yapayzekasozluk.tr "attention" tag page,
+ * entry "Sliding Window Attention"): the new query of sequence b, at position
+ * seq_lens[b] - 1, sees only the cached tokens within `window` positions
+ * before it, i.e. logical tokens max(0, len - 1 - window) .. len - 1; window
+ * < 0 means every cached token (then this equals oracle_decode_paged_rows).
+ * Page lookup, layouts and the row list as oracle_decode_paged_rows.
+ */
+int oracle_decode_paged_window_rows(const float *q, const float *k_cache, const float *v_cache,
+                                    const int32_t *page_table, const int32_t *seq_lens,
+                                    int B, int Hq, int Hkv, int d, int page_size,
+                                    int num_pages, int maxp, int window, double scale,
+                                    const int32_t *seqs, int nseq,
+                                    double *o_rows, double *lse_rows, int nthreads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0)
+        return -1;
+    const int group = Hq / Hkv;
+    const int nt = set_threads(nthreads);
+    int64_t maxlen = 0;
+    for (int r = 0; r < nseq; ++r) {
+        const int b = seqs[r];
+        if (b < 0 || b >= B) return -1;
+        const int64_t len = seq_lens[b];
+        if (len < 0 || len > (int64_t)maxp * page_size) return -1;
+        const int64_t first = (window >= 0 && len - 1 - window > 0) ? len - 1 - window : 0;
+        for (int64_t p = first / page_size; p < (len + page_size - 1) / page_size; ++p) {
+            const int32_t pid = page_table[(int64_t)b * maxp + p];
+            if (pid < 0 || pid >= num_pages) return -1;
+        }
+        if (len > maxlen) maxlen = len;
+    }
+#pragma omp parallel num_threads(nt)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+        const float **kr = (const float **)malloc(sizeof(float *) * (size_t)(maxlen > 0 ? maxlen : 1));
+        const float **vr = (const float **)malloc(sizeof(float *) * (size_t)(maxlen > 0 ? maxlen : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t rr = 0; rr < (int64_t)nseq * Hq; ++rr) {
+            const int r = (int)(rr / Hq);
+            const int h = (int)(rr % Hq);
+            const int b = seqs[r];
+            const int g = h / group;
+            const int64_t len = seq_lens[b];
+            const int64_t first = (window >= 0 && len - 1 - window > 0) ? len - 1 - window : 0;
+            for (int64_t t = first; t < len; ++t) {
+                const int64_t page = page_table[(int64_t)b * maxp + t / page_size];
+                const int64_t off = ((page * page_size + t % page_size) * Hkv + g) * d;
+                kr[t - first] = k_cache + off;
+                vr[t - first] = v_cache + off;
+            }
+            attention_row(q + ((int64_t)b * Hq + h) * d, kr, vr, len - first, d, scale, s,
+                          o_rows + rr * d, lse_rows + rr);
+        }
+        free(s);
+        free(kr);
+        free(vr);
+    }
+    return 0;
+}
+
+/*
  * The pages' online softmax statistics, in their order ("Donanıma Duyarlı
  * Algoritma Tasarımı: FlashAttention", section "Online Softmax Prensibi",
  * steps 1-5).  The row x[0..n) is consumed in blocks of `block` values.  For

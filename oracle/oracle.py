@@ -54,13 +54,15 @@ def _load():
         lib.oracle_attn_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, D, I]
         lib.oracle_decode_paged_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D,
                                                  P, I, P, P, I]
+        lib.oracle_decode_paged_window_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I,
+                                                        D, P, I, P, P, I]
         lib.oracle_online_softmax_stats.argtypes = [P, I64, I64, P, P]
         lib.oracle_online_softmax_stats.restype = None
         lib.oracle_merge_parts.argtypes = [P, P, I, I, P, P]
         lib.oracle_merge_parts.restype = None
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_attn_varlen",
-                     "oracle_attn_window_rows",
+                     "oracle_attn_window_rows", "oracle_decode_paged_window_rows",
                      "oracle_decode_paged_rows", "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -190,6 +192,27 @@ def decode_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float, seqs=N
                                           _p(o), _p(lse), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_decode_paged_rows rejected its arguments")
+    return o, lse
+
+
+def decode_paged_window(q, k_cache, v_cache, page_table, seq_lens, window: int, scale: float,
+                        seqs=None, nthreads: int = 0):
+    """Decode where the query of sequence b sees only its last window + 1 cached tokens
+    (window < 0: all).  Arguments and results as decode_paged."""
+    q, kc, vc = _f32(q), _f32(k_cache), _f32(v_cache)
+    pt, sl = _i32(page_table), _i32(seq_lens)
+    B, Hq, d = q.shape
+    P, ps, Hkv, _ = kc.shape
+    maxp = pt.shape[1]
+    seqs = _i32(np.arange(B) if seqs is None else seqs)
+    n = seqs.shape[0]
+    o = np.zeros((n, Hq, d), np.float64)
+    lse = np.zeros((n, Hq), np.float64)
+    rc = _load().oracle_decode_paged_window_rows(_p(q), _p(kc), _p(vc), _p(pt), _p(sl), B, Hq,
+                                                 Hkv, d, ps, P, maxp, int(window), float(scale),
+                                                 _p(seqs), n, _p(o), _p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_paged_window_rows rejected its arguments")
     return o, lse
 
 

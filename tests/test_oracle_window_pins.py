@@ -96,3 +96,56 @@ def test_window_brute_force_tiny(oracle, N, Hq, Hkv, d, wl, wr):
     ob, lb = _brute_window(q, k, v, wl, wr, 0.8, Hq // Hkv)
     np.testing.assert_allclose(o, ob, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(lse, lb, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- windowed decode
+
+def _paged_case(lens, Hq, Hkv, d, seed):
+    from attn_fwd_07_b300 import inputs
+    p = inputs.paged(lens, Hq, Hkv, d, seed, page_size=16)
+    return tuple(t.float().numpy() for t in (p.q, p.k_cache, p.v_cache)) + (
+        p.page_table.numpy(), p.seq_lens.numpy(), p.scale)
+
+
+def test_decode_window_wide_equals_decode(oracle):
+    """A window reaching back to token 0 (or -1) sees every cached token: the plain
+    paged decode entry point.  Catches: a window that drops the first or last page."""
+    q, kc, vc, pt, sl, sc = _paged_case([1, 17, 40, 100], 8, 2, 16, 21)
+    o0, l0 = oracle.decode_paged(q, kc, vc, pt, sl, sc)
+    for window in (-1, 99, 1000):
+        o, l = oracle.decode_paged_window(q, kc, vc, pt, sl, window, sc)
+        np.testing.assert_array_equal(o, o0)
+        np.testing.assert_array_equal(l, l0)
+
+
+def test_decode_window_zero_is_last_value(oracle):
+    """window = 0: the query sees only the newest token, so O = its V row and
+    LSE = its score.  Catches: an off-by-one at the newest token."""
+    q, kc, vc, pt, sl, sc = _paged_case([1, 16, 33, 70], 4, 2, 8, 22)
+    o, l = oracle.decode_paged_window(q, kc, vc, pt, sl, 0, sc)
+    for b, n in enumerate(sl):
+        t = n - 1
+        page, slot = pt[b, t // 16], t % 16
+        for h in range(4):
+            g = h // 2
+            np.testing.assert_array_equal(o[b, h], vc[page, slot, g].astype(np.float64))
+            s = sc * float(np.dot(q[b, h].astype(np.float64), kc[page, slot, g].astype(np.float64)))
+            assert l[b, h] == pytest.approx(s, abs=1e-13)
+
+
+def test_decode_window_equals_last_row_of_window_prefill(oracle):
+    """The windowed decode of a sequence equals the last row of windowed prefill
+    (window_left = window, window_right = 0) over the same keys laid out densely.
+    Catches: a window measured from the wrong end, a wrong page of the window."""
+    lens = [50, 77]
+    q, kc, vc, pt, sl, sc = _paged_case(lens, 4, 2, 8, 23)
+    for window in (0, 5, 16, 31, 49):
+        o, l = oracle.decode_paged_window(q, kc, vc, pt, sl, window, sc)
+        for b, n in enumerate(sl):
+            kd = np.stack([kc[pt[b, t // 16], t % 16] for t in range(n)])[None]
+            vd = np.stack([vc[pt[b, t // 16], t % 16] for t in range(n)])[None]
+            qd = np.zeros((1, n, 4, 8), np.float32)
+            qd[0, n - 1] = q[b]
+            od, ld = oracle.attn_window(qd, kd, vd, window, 0, sc)
+            np.testing.assert_allclose(o[b], od[0, n - 1], rtol=0, atol=1e-14)
+            np.testing.assert_allclose(l[b], ld[0, :, n - 1], rtol=0, atol=1e-13)
