@@ -298,10 +298,16 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_p
     return ((bytes_o + 255) & ~(size_t)255) + bytes_l;
 }
 
-attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+}  // extern "C"
+
+namespace {
+
+// The paged decode behind attn_decode_paged (window = -1) and
+// attn_decode_paged_window (the query sees the last window + 1 tokens).
+attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *v_cache,
                                 const int32_t *page_table, const int32_t *seq_lens, void *o,
                                 float *lse, int B, int Hq, int Hkv, int d, int page_size,
-                                int num_pages, int max_pages_per_seq, float scale,
+                                int num_pages, int max_pages_per_seq, int window, float scale,
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream) {
     if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o || !workspace)
         return ATTN_ERR_INVALID_ARG;
@@ -353,6 +359,7 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
     p.num_pages = num_pages;
     p.maxp = max_pages_per_seq;
     p.stages = stages;
+    p.window = window < 0 ? -1 : window;
     p.scale_log2 = scale * kLog2e;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const int G = st->sms;
@@ -361,6 +368,32 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
     if ((s = launch_status()) != ATTN_OK) return s;
     decode_merge_kernel<<<B, 256, 0, cs>>>(p, G);
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *page_table, const int32_t *seq_lens, void *o,
+                                float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                                int num_pages, int max_pages_per_seq, float scale,
+                                void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+    return decode_paged_impl(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
+                             page_size, num_pages, max_pages_per_seq, -1, scale, workspace,
+                             workspace_bytes, stream);
+}
+
+attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const void *v_cache,
+                                       const int32_t *page_table, const int32_t *seq_lens,
+                                       void *o, float *lse, int B, int Hq, int Hkv, int d,
+                                       int page_size, int num_pages, int max_pages_per_seq,
+                                       int window, float scale, void *workspace,
+                                       size_t workspace_bytes, attn_stream_t stream) {
+    if (window < -1) return ATTN_ERR_INVALID_ARG;
+    return decode_paged_impl(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
+                             page_size, num_pages, max_pages_per_seq, window, scale, workspace,
+                             workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- no-allocation decode

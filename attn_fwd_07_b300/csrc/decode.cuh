@@ -54,12 +54,14 @@ struct DecodeParams {
     unsigned *status;
     int B, Hq, Hkv, d, num_pages, maxp;
     int stages;
+    int window;                // the query sees the last window + 1 tokens; -1: all
     float scale_log2;
 };
 
 struct DecodeStageMeta {
     int b;        // sequence
-    int ntok;     // valid tokens in this page (0 if the page id was bad)
+    int lo;       // first valid token slot in this page (window start)
+    int ntok;     // valid token slots end here (0 if the page id was bad)
     int first;    // first page of a segment
     int last;     // last page of a segment
 };
@@ -77,10 +79,18 @@ inline size_t dec_smem_bytes(int Hkv, int d, int stages) {
     return 1024 /* alignment slack */ + (size_t)stages * dec_stage_bytes(Hkv, d) + dec_ctrl_bytes();
 }
 
-// ceil(len / 16) pages of sequence b
-__device__ __forceinline__ int dec_pages_of(const int32_t *seq_lens, int b) {
-    const int len = seq_lens[b];
-    return len > 0 ? (len + kDecPage - 1) / kDecPage : 0;
+// First token the query of sequence b attends to: len - 1 - window under a
+// window, else 0.
+__device__ __forceinline__ int dec_first_token(const DecodeParams &p, int b) {
+    const int len = p.seq_lens[b];
+    return (p.window >= 0 && len - 1 - p.window > 0) ? len - 1 - p.window : 0;
+}
+
+// Pages of sequence b that hold attended tokens: logical pages
+// first_token / 16 .. ceil(len / 16) - 1.
+__device__ __forceinline__ int dec_pages_of(const DecodeParams &p, int b) {
+    const int len = p.seq_lens[b];
+    return len > 0 ? (len + kDecPage - 1) / kDecPage - dec_first_token(p, b) / kDecPage : 0;
 }
 
 // The CTA whose page range [c*T/G, (c+1)*T/G) holds global page x.
@@ -133,7 +143,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
     long long T = 0;  // total pages of all sequences
     if (warp == Hkv) {
         for (int b0 = 0; b0 < p.B; b0 += 32) {
-            int np = (b0 + lane < p.B) ? dec_pages_of(p.seq_lens, b0 + lane) : 0;
+            int np = (b0 + lane < p.B) ? dec_pages_of(p, b0 + lane) : 0;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) np += __shfl_xor_sync(0xffffffffu, np, o);
             T += np;
@@ -161,13 +171,14 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         int np_b = 0;
         if (n_iter > 0) {
             for (;;) {
-                np_b = dec_pages_of(p.seq_lens, b);
+                np_b = dec_pages_of(p, b);
                 if (seq_start + np_b > p0) break;
                 seq_start += np_b;
                 ++b;
             }
         }
-        int lp = (int)(p0 - seq_start);   // logical page within sequence b
+        int lp = (int)(p0 - seq_start);   // page of sequence b, counted from its first
+        int fp_b = n_iter > 0 ? dec_first_token(p, b) / kDecPage : 0;  // first logical page
         int ids_base = -1;                // logical page of ids[lane] batch start
         int my_id = 0;
         const uint32_t tx = stage_bytes;
@@ -176,12 +187,14 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
             while (lp >= np_b) {
                 ++b;
                 lp = 0;
-                np_b = dec_pages_of(p.seq_lens, b);
+                np_b = dec_pages_of(p, b);
+                fp_b = dec_first_token(p, b) / kDecPage;
                 ids_base = -1;
             }
             if (ids_base < 0 || lp >= ids_base + 32) {
                 ids_base = lp;
-                my_id = (lp + lane < np_b) ? p.page_table[(long long)b * p.maxp + lp + lane] : 0;
+                my_id = (lp + lane < np_b)
+                            ? p.page_table[(long long)b * p.maxp + fp_b + lp + lane] : 0;
             }
             const int pid = __shfl_sync(0xffffffffu, my_id, lp - ids_base);
             const int s = it % S;
@@ -195,7 +208,9 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 const bool valid = (unsigned)pid < (unsigned)p.num_pages;
                 DecodeStageMeta mt;
                 mt.b = b;
-                mt.ntok = valid ? (last_of_seq ? p.seq_lens[b] - lp * kDecPage : kDecPage) : 0;
+                mt.ntok = valid ? (last_of_seq ? p.seq_lens[b] - (fp_b + lp) * kDecPage : kDecPage)
+                                : 0;
+                mt.lo = lp == 0 ? dec_first_token(p, b) - fp_b * kDecPage : 0;
                 mt.first = (it == 0 || lp == 0) ? 1 : 0;
                 mt.last = (it == n_iter - 1 || last_of_seq) ? 1 : 0;
                 meta[s] = mt;
@@ -288,10 +303,10 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 sv[2] = sacc[1][0] * p.scale_log2;
                 sv[3] = sacc[1][1] * p.scale_log2;
                 const int t0 = 2 * quad;
-                if (t0 >= mt.ntok) sv[0] = -INFINITY;
-                if (t0 + 1 >= mt.ntok) sv[1] = -INFINITY;
-                if (t0 + 8 >= mt.ntok) sv[2] = -INFINITY;
-                if (t0 + 9 >= mt.ntok) sv[3] = -INFINITY;
+                if (t0 >= mt.ntok || t0 < mt.lo) sv[0] = -INFINITY;
+                if (t0 + 1 >= mt.ntok || t0 + 1 < mt.lo) sv[1] = -INFINITY;
+                if (t0 + 8 >= mt.ntok || t0 + 8 < mt.lo) sv[2] = -INFINITY;
+                if (t0 + 9 >= mt.ntok || t0 + 9 < mt.lo) sv[3] = -INFINITY;
                 float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -375,7 +390,7 @@ decode_merge_kernel(const DecodeParams p, int G) {
     // start page of sequence b and total pages T
     long long before = 0, total = 0;
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
-        const int np = dec_pages_of(p.seq_lens, i);
+        const int np = dec_pages_of(p, i);
         total += np;
         if (i < b) before += np;
     }
@@ -396,7 +411,7 @@ decode_merge_kernel(const DecodeParams p, int G) {
         before += red[0][w];
         total += red[1][w];
     }
-    const int np = dec_pages_of(p.seq_lens, b);
+    const int np = dec_pages_of(p, b);
     const int dq = p.d / 4;
     if (np == 0) {
         for (int idx = threadIdx.x; idx < p.Hq * dq; idx += blockDim.x) {

@@ -158,6 +158,25 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_paged_window -- attn_decode_paged where the new query attends only
+ * to the last window + 1 cached tokens of its sequence (positions
+ * seq_lens[b] - 1 - window .. seq_lens[b] - 1): the decode side of local
+ * attention (yapayzekasozluk.tr "attention" tag page, entry "Sliding Window
+ * Attention": each token attends to a fixed window of neighbours, so per-token
+ * cost and the cache a step reads stay constant as the sequence grows).  Only
+ * the pages holding those tokens are read; the page table may still list the
+ * older pages.  window = -1 attends to every cached token (attn_decode_paged);
+ * window < -1 returns ATTN_ERR_INVALID_ARG.  Everything else as
+ * attn_decode_paged, including the workspace size.
+ */
+attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const void *v_cache,
+                                       const int32_t *page_table, const int32_t *seq_lens,
+                                       void *o, float *lse, int B, int Hq, int Hkv, int d,
+                                       int page_size, int num_pages, int max_pages_per_seq,
+                                       int window, float scale, void *workspace,
+                                       size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Bytes of workspace attn_decode_paged needs for these sizes (0 on invalid
  * sizes).  It depends only on B, Hq, d and the GPU's SM count, never on the
  * sequence lengths.

@@ -91,3 +91,48 @@ def test_workload_swa_n8192_sampled(oracle):
     og = f32(o)[0, i, h]
     lg = f32(lse)[0, h, i]
     assert_close(errors(og, o_ref, lg, lse_ref), "swa_n8192_w4096")
+
+
+# ---------------------------------------------------------------- windowed paged decode
+
+@pytest.mark.parametrize("lens,window", [
+    ([1, 15, 16, 17, 1023], 0), ([1, 15, 16, 17, 1023], 15), ([300, 2048, 4096], 16),
+    ([300, 2048, 4096], 1000), ([5000, 33, 700, 12000], 4095), ([40, 41], 100000),
+])
+def test_decode_window_small(oracle, lens, window):
+    p = inputs.paged(lens, 32, 8, 128, 4000 + window % 997 + len(lens), page_size=16)
+    o, lse = A.attn_decode_paged_window(*(t.cuda() for t in (p.q, p.k_cache, p.v_cache,
+                                                              p.page_table, p.seq_lens)),
+                                        window, p.scale)
+    torch.cuda.synchronize()
+    check_status()
+    o_ref, lse_ref = oracle.decode_paged_window(*(f32(t) for t in (p.q, p.k_cache, p.v_cache)),
+                                                p.page_table.numpy(), p.seq_lens.numpy(),
+                                                window, p.scale)
+    assert_close(errors(f32(o), o_ref, f32(lse), lse_ref), (lens, window))
+
+
+def test_decode_window_minus_one_is_plain_decode():
+    """window = -1 is attn_decode_paged: bitwise the same split plan and results."""
+    p = inputs.paged([100, 2000, 5], 16, 4, 128, 4100, page_size=16)
+    args = [t.cuda() for t in (p.q, p.k_cache, p.v_cache, p.page_table, p.seq_lens)]
+    o1, l1 = A.attn_decode_paged_window(*args, -1, p.scale)
+    o2, l2 = A.attn_decode_paged(*args, p.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    check_status()
+
+
+def test_decode_window_workload_sampled(oracle):
+    """The 64-sequence decode workload with a 4096-token window, on 8 sequences."""
+    w = inputs.make("decode_paged_b64")
+    o, lse = A.attn_decode_paged_window(*(t.cuda() for t in (w.q, w.k_cache, w.v_cache,
+                                                              w.page_table, w.seq_lens)),
+                                        4095, w.scale)
+    torch.cuda.synchronize()
+    check_status()
+    seqs = np.array([0, 5, 17, 23, 31, 40, 52, 63], np.int32)
+    o_ref, lse_ref = oracle.decode_paged_window(*(f32(t) for t in (w.q, w.k_cache, w.v_cache)),
+                                                w.page_table.numpy(), w.seq_lens.numpy(), 4095,
+                                                w.scale, seqs=seqs)
+    assert_close(errors(f32(o)[seqs], o_ref, f32(lse)[seqs], lse_ref), "decode window 4095")
