@@ -177,6 +177,55 @@ def paged(lens, Hq, Hkv, d, seed, page_size=16, max_pages=None, dtype=torch.bflo
 
 
 @dataclass
+class PagedFP8:
+    q: torch.Tensor           # [B, Hq, d] bf16
+    k_cache: torch.Tensor     # [P, page_size, Hkv, d] uint8 (FP8 E4M3 bytes)
+    v_cache: torch.Tensor
+    k_scale: torch.Tensor     # [Hkv] float32: element c of head g stands for scale[g] * e4m3
+    v_scale: torch.Tensor
+    page_table: torch.Tensor  # int32 [B, maxp]
+    seq_lens: torch.Tensor    # int32 [B]
+    scale: float
+
+
+def _to_e4m3(x: torch.Tensor):
+    """float32 [P, ps, Hkv, d] -> (E4M3 bytes, per-head float32 scales) with each head's
+    largest magnitude mapped to 448, the largest E4M3 value (torch's float8_e4m3fn cast,
+    round to nearest even)."""
+    amax = x.abs().amax(dim=(0, 1, 3)).clamp_min(1e-30)
+    sc = (amax / 448.0).to(torch.float32)
+    q8 = (x / sc.view(1, 1, -1, 1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return q8.view(torch.uint8).contiguous(), sc
+
+
+def paged_fp8(lens, Hq, Hkv, d, seed, page_size=16, max_pages=None, factor=1.0,
+              scale=None) -> PagedFP8:
+    """The paged recipe above with the cache held as FP8 E4M3 bytes and one scale per
+    key/value head for K and for V: the same float32 draws, divided by the head's scale
+    and rounded to E4M3 (as a cache writer that quantises on append would)."""
+    lens = np.asarray(lens, np.int64)
+    B = len(lens)
+    npages = (lens + page_size - 1) // page_size
+    pool = int(npages.sum())
+    maxp = int(npages.max()) if max_pages is None else int(max_pages)
+    assert maxp >= int(npages.max())
+    perm = np.random.default_rng([seed, TAG_PERM]).permutation(pool).astype(np.int32)
+    table = np.full((B, maxp), -1, np.int32)
+    off = 0
+    for b in range(B):
+        table[b, :npages[b]] = perm[off:off + npages[b]]
+        off += npages[b]
+    q = normal_tensor((B, Hq, d), seed, TAG_Q, torch.bfloat16, factor)
+    kc, ks = _to_e4m3(normal_tensor((pool, page_size, Hkv, d), seed, TAG_K, torch.float32,
+                                    factor))
+    vc, vs = _to_e4m3(normal_tensor((pool, page_size, Hkv, d), seed, TAG_V, torch.float32,
+                                    factor))
+    return PagedFP8(q, kc, vc, ks, vs, torch.from_numpy(table),
+                    torch.from_numpy(lens.astype(np.int32)),
+                    (1.0 / math.sqrt(d)) if scale is None else scale)
+
+
+@dataclass
 class Workload:
     name: str
     kind: str                 # "dense" | "varlen" | "decode"
@@ -212,6 +261,13 @@ WORKLOADS = {
         dict(B=1, N=8192, Hq=32, Hkv=8, d=128, dtype=torch.bfloat16, factor=1.0,
              window=(2048, 2048)),
         "B=1 Hq=32 Hkv=8 N=8192 d=128, bf16 N(0,1), sliding window of 2048 keys left and right"),
+    # the decode workload with the cache quantised to FP8 E4M3 (one scale per key/value
+    # head), the INT8/FP8 cache the KV-cache glossary entry mentions
+    "decode_paged_fp8_b64": Workload(
+        "decode_paged_fp8_b64", "decode_fp8", 5,
+        dict(B=64, lo=1024, hi=32768, Hq=32, Hkv=8, d=128, page_size=16, factor=1.0),
+        "B=64 one query each, lengths U[1024,32768], Hq=32 Hkv=8 d=128, 16-token pages, "
+        "permuted page table, N(0,1) cache quantised to FP8 E4M3 with per-head scales"),
     "decode_paged_b64": Workload(
         "decode_paged_b64", "decode", 5,
         dict(B=64, lo=1024, hi=32768, Hq=32, Hkv=8, d=128, page_size=16,
@@ -249,4 +305,10 @@ def make(name: str, batch: int | None = None):
         maxp = (p["hi"] + p["page_size"] - 1) // p["page_size"]
         return paged(lens, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"], maxp, p["dtype"],
                      p["factor"])
+    if w.kind == "decode_fp8":
+        B = p["B"] if batch is None else int(batch)
+        lens = lengths(B, p["lo"], p["hi"], w.seed)
+        maxp = (p["hi"] + p["page_size"] - 1) // p["page_size"]
+        return paged_fp8(lens, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"], maxp,
+                         p["factor"])
     raise ValueError(w.kind)

@@ -427,6 +427,112 @@ int oracle_decode_paged_window_rows(const float *q, const float *k_cache, const 
 }
 
 /*
+ * The value of one FP8 E4M3 byte (OCP 8-bit floating point, "E4M3FN": 1 sign
+ * bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities; exponent
+ * and mantissa all ones is NaN):
+ *     e = 0:   (-1)^s * (m / 8) * 2^(1 - 7)        (subnormal, includes zero)
+ *     e > 0:   (-1)^s * (1 + m / 8) * 2^(e - 7)
+ */
+double oracle_e4m3_value(uint8_t x)
+{
+    const int sgn = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m / 8.0, 1 - 7) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sgn ? -mag : mag;
+}
+
+/*
+ * Decode against a paged cache held as FP8 E4M3 bytes (yapayzekasozluk.tr
+ * "attention" tag page, entry "KV Cache": the cache may be kept in INT8/FP8 to
+ * cut its memory 2-4x).  Cached key (value) element c of head g stands for
+ * k_scale[g] * e4m3(byte) (v_scale[g] * e4m3(byte)); the query attends to
+ * those dequantised values exactly as in oracle_decode_paged_rows.  The bytes
+ * are dequantised here in fp64, row by row, into scratch rows.
+ */
+int oracle_decode_paged_fp8_rows(const float *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *page_table, const int32_t *seq_lens,
+                                 int B, int Hq, int Hkv, int d, int page_size,
+                                 int num_pages, int maxp, double scale,
+                                 const int32_t *seqs, int nseq,
+                                 double *o_rows, double *lse_rows, int nthreads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0)
+        return -1;
+    const int group = Hq / Hkv;
+    const int nt = set_threads(nthreads);
+    int64_t maxlen = 0;
+    for (int r = 0; r < nseq; ++r) {
+        const int b = seqs[r];
+        if (b < 0 || b >= B) return -1;
+        const int64_t len = seq_lens[b];
+        if (len < 0 || len > (int64_t)maxp * page_size) return -1;
+        for (int64_t p = 0; p < (len + page_size - 1) / page_size; ++p) {
+            const int32_t pid = page_table[(int64_t)b * maxp + p];
+            if (pid < 0 || pid >= num_pages) return -1;
+        }
+        if (len > maxlen) maxlen = len;
+    }
+    const int64_t cap = maxlen > 0 ? maxlen : 1;
+#pragma omp parallel num_threads(nt)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)cap);
+        /* dequantised key/value rows in fp64 (k_scale * e4m3 is not always a float,
+         * so the definition is written out again below on double rows instead of
+         * going through attention_row, which reads float rows) */
+        double *kd = (double *)malloc(sizeof(double) * (size_t)cap * d);
+        double *vd = (double *)malloc(sizeof(double) * (size_t)cap * d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t rr = 0; rr < (int64_t)nseq * Hq; ++rr) {
+            const int r = (int)(rr / Hq);
+            const int h = (int)(rr % Hq);
+            const int b = seqs[r];
+            const int g = h / group;
+            const int64_t len = seq_lens[b];
+            double *orow = o_rows + rr * d;
+            if (len == 0) {
+                for (int c = 0; c < d; ++c) orow[c] = 0.0;
+                lse_rows[rr] = -INFINITY;
+                continue;
+            }
+            for (int64_t t = 0; t < len; ++t) {
+                const int64_t page = page_table[(int64_t)b * maxp + t / page_size];
+                const int64_t off = ((page * page_size + t % page_size) * Hkv + g) * d;
+                for (int c = 0; c < d; ++c) {
+                    kd[t * d + c] = (double)k_scale[g] * oracle_e4m3_value(k_cache[off + c]);
+                    vd[t * d + c] = (double)v_scale[g] * oracle_e4m3_value(v_cache[off + c]);
+                }
+            }
+            /* the definition, as in attention_row, on the dequantised rows */
+            const float *qr = q + ((int64_t)b * Hq + h) * d;
+            for (int64_t t = 0; t < len; ++t) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += (double)qr[c] * kd[t * d + c];
+                s[t] = scale * acc;
+            }
+            double m = s[0];
+            for (int64_t t = 1; t < len; ++t)
+                if (s[t] > m) m = s[t];
+            double l = 0.0;
+            for (int64_t t = 0; t < len; ++t) {
+                s[t] = exp(s[t] - m);
+                l += s[t];
+            }
+            for (int c = 0; c < d; ++c) orow[c] = 0.0;
+            for (int64_t t = 0; t < len; ++t) {
+                const double pw = s[t] / l;
+                for (int c = 0; c < d; ++c) orow[c] += pw * vd[t * d + c];
+            }
+            lse_rows[rr] = m + log(l);
+        }
+        free(s);
+        free(kd);
+        free(vd);
+    }
+    return 0;
+}
+
+/*
  * The pages' online softmax statistics, in their order ("Donanıma Duyarlı
  * Algoritma Tasarımı: FlashAttention", section "Online Softmax Prensibi",
  * steps 1-5).  The row x[0..n) is consumed in blocks of `block` values.  For

@@ -56,6 +56,10 @@ def _load():
                                                  P, I, P, P, I]
         lib.oracle_decode_paged_window_rows.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I,
                                                         D, P, I, P, P, I]
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = D
+        lib.oracle_decode_paged_fp8_rows.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, D,
+                                                     P, I, P, P, I]
         lib.oracle_online_softmax_stats.argtypes = [P, I64, I64, P, P]
         lib.oracle_online_softmax_stats.restype = None
         lib.oracle_merge_parts.argtypes = [P, P, I, I, P, P]
@@ -63,6 +67,7 @@ def _load():
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_attn_varlen",
                      "oracle_attn_window_rows", "oracle_decode_paged_window_rows",
+                     "oracle_decode_paged_fp8_rows",
                      "oracle_decode_paged_rows", "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -213,6 +218,37 @@ def decode_paged_window(q, k_cache, v_cache, page_table, seq_lens, window: int, 
                                                  _p(seqs), n, _p(o), _p(lse), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_decode_paged_window_rows rejected its arguments")
+    return o, lse
+
+
+def e4m3_value(byte: int) -> float:
+    """The value of one FP8 E4M3 (E4M3FN) byte, from its bit fields."""
+    return float(_load().oracle_e4m3_value(int(byte) & 0xFF))
+
+
+def decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                     scale: float, seqs=None, nthreads: int = 0):
+    """Decode against an FP8 E4M3 paged cache: k_cache/v_cache uint8 [P,page_size,Hkv,d]
+    (E4M3 bytes), k_scale/v_scale [Hkv] (element c of head g stands for scale[g] *
+    e4m3(byte)).  Other arguments and results as decode_paged."""
+    q = _f32(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    pt, sl = _i32(page_table), _i32(seq_lens)
+    B, Hq, d = q.shape
+    P, ps, Hkv, _ = kc.shape
+    assert vc.shape == kc.shape and ks.shape == (Hkv,) and vs.shape == (Hkv,)
+    maxp = pt.shape[1]
+    seqs = _i32(np.arange(B) if seqs is None else seqs)
+    n = seqs.shape[0]
+    o = np.zeros((n, Hq, d), np.float64)
+    lse = np.zeros((n, Hq), np.float64)
+    rc = _load().oracle_decode_paged_fp8_rows(_p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(pt),
+                                              _p(sl), B, Hq, Hkv, d, ps, P, maxp, float(scale),
+                                              _p(seqs), n, _p(o), _p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_paged_fp8_rows rejected its arguments")
     return o, lse
 
 
