@@ -17,7 +17,7 @@ import torch
 
 __all__ = [
     "AttnError", "load_library", "attn_fwd", "attn_fwd_window", "attn_fwd_f32",
-    "attn_fwd_varlen", "attn_decode_paged", "attn_decode_paged_window",
+    "attn_fwd_varlen", "attn_decode_paged", "attn_decode_paged_window", "attn_decode_paged_fp8",
     "attn_decode_paged_noalloc", "attn_decode_workspace_size", "attn_status_string",
     "attn_get_device_status", "attn_version", "attn_last_cuda_error",
 ]
@@ -58,6 +58,8 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]
+        lib.attn_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
+                                              P, SZ, P]
         lib.attn_decode_paged_window.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                                  P, SZ, P]
         lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
@@ -72,7 +74,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_last_cuda_error.argtypes = []
         lib.attn_last_cuda_error.restype = ctypes.c_char_p
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
-                     "attn_fwd_window", "attn_decode_paged_window",
+                     "attn_fwd_window", "attn_decode_paged_window", "attn_decode_paged_fp8",
                      "attn_decode_paged_noalloc", "attn_get_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -237,6 +239,39 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | 
                                           workspace.numel() * workspace.element_size(),
                                           _stream(stream))
     _check(rc, "attn_decode_paged")
+    return o, lse
+
+
+def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                          scale: float | None = None, o=None, lse=None, workspace=None,
+                          want_lse: bool = True, stream=None):
+    """Decode against an FP8 E4M3 paged cache: k_cache/v_cache uint8 [P,page,Hkv,d] holding
+    E4M3 bytes, k_scale/v_scale float32 [Hkv] per-head scales.  q, page_table, seq_lens and
+    the results as attn_decode_paged."""
+    _need(q, torch.bfloat16, "q")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.uint8, n)
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, torch.float32, n)
+    _need(page_table, torch.int32, "page_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, d = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    maxp = page_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = attn_decode_workspace_size(B, Hq, Hkv, d, maxp, ps)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = load_library().attn_decode_paged_fp8(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
+        _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, ps, P, maxp, float(scale),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_decode_paged_fp8")
     return o, lse
 
 

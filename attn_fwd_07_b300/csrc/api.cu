@@ -85,7 +85,11 @@ attn_status_t device_state(DeviceState **out) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)PrefillCfg<64>::SMEM)) != cudaSuccess)
             return cuda_fail(e);
-        if ((e = cudaFuncSetAttribute(decode_split_kernel,
+        if ((e = cudaFuncSetAttribute(decode_split_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      227 * 1024)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaFuncSetAttribute(decode_split_kernel<false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       227 * 1024)) != cudaSuccess)
             return cuda_fail(e);
@@ -105,9 +109,10 @@ attn_status_t device_state(DeviceState **out) {
 
 // bf16 tensor map, 128-byte swizzle, box inner extent 64 elements.
 attn_status_t make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims,
-                       const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+                       const cuuint64_t *strides_bytes, const cuuint32_t *box,
+                       CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
+    CUresult r = g_encode(m, dtype, (cuuint32_t)rank,
                           const_cast<void *>(ptr), dims, strides_bytes, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -302,15 +307,19 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_p
 
 namespace {
 
-// The paged decode behind attn_decode_paged (window = -1) and
-// attn_decode_paged_window (the query sees the last window + 1 tokens).
+// The paged decode behind attn_decode_paged (window = -1), attn_decode_paged_window
+// (the query sees the last window + 1 tokens) and attn_decode_paged_fp8 (k_scale,
+// v_scale non-null: the cache holds FP8 E4M3 bytes).
 attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *v_cache,
+                                const float *k_scale, const float *v_scale,
                                 const int32_t *page_table, const int32_t *seq_lens, void *o,
                                 float *lse, int B, int Hq, int Hkv, int d, int page_size,
                                 int num_pages, int max_pages_per_seq, int window, float scale,
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+    const bool fp8 = k_scale != nullptr;
     if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o || !workspace)
         return ATTN_ERR_INVALID_ARG;
+    if (fp8 && !v_scale) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 ||
         num_pages <= 0 || max_pages_per_seq <= 0)
         return ATTN_ERR_INVALID_ARG;
@@ -320,26 +329,31 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
         return ATTN_ERR_INVALID_ARG;
     if (page_size != kDecPage || (d != 64 && d != 128) || Hkv > kDecMaxHkv || Hq / Hkv > 8)
         return ATTN_ERR_UNSUPPORTED;
+    if (fp8 && d != 128) return ATTN_ERR_UNSUPPORTED;
     const size_t need = attn_decode_workspace_size(B, Hq, Hkv, d, max_pages_per_seq, page_size);
     if (need == 0) return ATTN_ERR_CUDA;
     if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
     DeviceState *st = nullptr;
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
-    const size_t stage = dec_stage_bytes(Hkv, d);
+    const size_t stage = dec_stage_bytes(Hkv, d, fp8);
     int stages = (int)((220 * 1024 - 2048) / stage);
     if (stages > kDecMaxStages) stages = kDecMaxStages;
     if (stages < 2) return ATTN_ERR_UNSUPPORTED;
     // cache as a 4-D tensor: (dim, token-in-page, head, page) so that one box
-    // lands in shared memory as [head][token][64 dims]
+    // lands in shared memory as [head][token][128-byte row]: 64 bf16 dims per box,
+    // or all 128 E4M3 dims
+    const cuuint64_t esz = fp8 ? 1 : 2;
     const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)Hkv,
                                 (cuuint64_t)num_pages};
-    const cuuint64_t strides[3] = {(cuuint64_t)Hkv * d * 2, (cuuint64_t)d * 2,
-                                   (cuuint64_t)page_size * Hkv * d * 2};
-    const cuuint32_t box[4] = {64, (cuuint32_t)page_size, (cuuint32_t)Hkv, 1};
+    const cuuint64_t strides[3] = {(cuuint64_t)Hkv * d * esz, (cuuint64_t)d * esz,
+                                   (cuuint64_t)page_size * Hkv * d * esz};
+    const cuuint32_t box[4] = {fp8 ? 128u : 64u, (cuuint32_t)page_size, (cuuint32_t)Hkv, 1};
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap mk, mv;
-    if ((s = make_map(&mk, k_cache, 4, dims, strides, box)) != ATTN_OK) return s;
-    if ((s = make_map(&mv, v_cache, 4, dims, strides, box)) != ATTN_OK) return s;
+    if ((s = make_map(&mk, k_cache, 4, dims, strides, box, dt)) != ATTN_OK) return s;
+    if ((s = make_map(&mv, v_cache, 4, dims, strides, box, dt)) != ATTN_OK) return s;
 
     const size_t slots = (size_t)B + (size_t)st->sms;
     DecodeParams p;
@@ -351,6 +365,8 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
                                            ((slots * Hq * d * sizeof(float) + 255) & ~(size_t)255));
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     p.status = st->status;
     p.B = B;
     p.Hq = Hq;
@@ -363,8 +379,11 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     p.scale_log2 = scale * kLog2e;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const int G = st->sms;
-    const size_t smem = dec_smem_bytes(Hkv, d, stages);
-    decode_split_kernel<<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
+    const size_t smem = dec_smem_bytes(Hkv, d, stages, fp8);
+    if (fp8)
+        decode_split_kernel<true><<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
+    else
+        decode_split_kernel<false><<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
     if ((s = launch_status()) != ATTN_OK) return s;
     decode_merge_kernel<<<B, 256, 0, cs>>>(p, G);
     return launch_status();
@@ -379,9 +398,23 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
                                 float *lse, int B, int Hq, int Hkv, int d, int page_size,
                                 int num_pages, int max_pages_per_seq, float scale,
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream) {
-    return decode_paged_impl(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
+    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, page_table, seq_lens, o, lse,
+                             B, Hq, Hkv, d,
                              page_size, num_pages, max_pages_per_seq, -1, scale, workspace,
                              workspace_bytes, stream);
+}
+
+attn_status_t attn_decode_paged_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                    const float *k_scale, const float *v_scale,
+                                    const int32_t *page_table, const int32_t *seq_lens, void *o,
+                                    float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                                    int num_pages, int max_pages_per_seq, float scale,
+                                    void *workspace, size_t workspace_bytes,
+                                    attn_stream_t stream) {
+    if (!k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
+    return decode_paged_impl(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, o, lse,
+                             B, Hq, Hkv, d, page_size, num_pages, max_pages_per_seq, -1, scale,
+                             workspace, workspace_bytes, stream);
 }
 
 attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const void *v_cache,
@@ -391,7 +424,8 @@ attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const
                                        int window, float scale, void *workspace,
                                        size_t workspace_bytes, attn_stream_t stream) {
     if (window < -1) return ATTN_ERR_INVALID_ARG;
-    return decode_paged_impl(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
+    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, page_table, seq_lens, o, lse,
+                             B, Hq, Hkv, d,
                              page_size, num_pages, max_pages_per_seq, window, scale, workspace,
                              workspace_bytes, stream);
 }

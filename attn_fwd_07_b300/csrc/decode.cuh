@@ -51,6 +51,8 @@ struct DecodeParams {
     float *part_lse;           // [B + G, Hq]
     __nv_bfloat16 *o;          // [B, Hq, d]
     float *lse;                // [B, Hq] or null
+    const float *k_scale;      // FP8 cache: [Hkv] per-head scales of K and V; else null
+    const float *v_scale;
     unsigned *status;
     int B, Hq, Hkv, d, num_pages, maxp;
     int stages;
@@ -67,16 +69,18 @@ struct DecodeStageMeta {
 };
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base):
-//   stage s:  K half 0 .. K half (d/64 - 1), V half 0 .. V half (d/64 - 1),
-//             each [Hkv][16][64] bf16 = Hkv * 2048 bytes
-//   then full[kDecMaxStages], empty[kDecMaxStages] mbarriers, meta, scalars.
+//   stage s:  bf16 cache: K half 0 .. K half (d/64 - 1), V half 0 .. V half (d/64 - 1),
+//             each [Hkv][16][64] bf16 = Hkv * 2048 bytes;
+//             FP8 cache (d = 128): K, then V, each [Hkv][16][128] bytes = Hkv * 2048
+//   then full[kDecMaxStages], empty[kDecMaxStages] mbarriers, meta, scalars (1 KB).
 __host__ __device__ inline uint32_t dec_half_bytes(int Hkv) { return (uint32_t)Hkv * 16u * 128u; }
-__host__ __device__ inline uint32_t dec_stage_bytes(int Hkv, int d) {
-    return 2u * (uint32_t)(d / 64) * dec_half_bytes(Hkv);
+__host__ __device__ inline uint32_t dec_stage_bytes(int Hkv, int d, bool fp8) {
+    return 2u * (fp8 ? 1u : (uint32_t)(d / 64)) * dec_half_bytes(Hkv);
 }
 __host__ __device__ inline uint32_t dec_ctrl_bytes() { return 1024u; }
-inline size_t dec_smem_bytes(int Hkv, int d, int stages) {
-    return 1024 /* alignment slack */ + (size_t)stages * dec_stage_bytes(Hkv, d) + dec_ctrl_bytes();
+inline size_t dec_smem_bytes(int Hkv, int d, int stages, bool fp8) {
+    return 1024 /* alignment slack */ + (size_t)stages * dec_stage_bytes(Hkv, d, fp8) +
+           dec_ctrl_bytes();
 }
 
 // First token the query of sequence b attends to: len - 1 - window under a
@@ -105,6 +109,12 @@ __host__ __device__ __forceinline__ bool dec_range_nonempty(long long c, long lo
     return (c + 1) * T / G > c * T / G;
 }
 
+// FP8: the cache holds E4M3 bytes.  Each consumer lane reads the bytes of its MMA
+// fragments straight from the stage (the contraction's k order and the output's
+// column order are permuted so that they are contiguous 16-byte chunks), widens
+// them to f16 (exact) and runs the products with f16 operands; per-head scales
+// multiply the scores and the output.
+template <bool FP8>
 __global__ void __launch_bounds__(32 * (kDecMaxHkv + 1), 1)
 decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
@@ -114,9 +124,9 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
     uint8_t *base_ptr = dec_smem_raw + (base - raw);
 
     const int S = p.stages;
-    const uint32_t stage_bytes = dec_stage_bytes(p.Hkv, p.d);
+    const uint32_t stage_bytes = dec_stage_bytes(p.Hkv, p.d, FP8);
     const uint32_t half_bytes = dec_half_bytes(p.Hkv);
-    const int nhalf = p.d / 64;
+    const int nhalf = FP8 ? 1 : p.d / 64;   // TMA boxes per tensor and page
     const uint32_t ctrl = base + (uint32_t)S * stage_bytes;
     uint8_t *ctrl_ptr = base_ptr + (size_t)S * stage_bytes;
     // control block: full[4] @0, empty[4] @32, meta[4] @64, scalars @192
@@ -240,8 +250,15 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         const int nk = p.d / 16;               // k-steps of S = q K^T
         const int nd = p.d / 8;                // n-tiles of O
 
-        uint32_t qa[8][2];                     // A fragments of q (rows 0..7)
+        // A fragments of q (rows 0..7).  FP8 cache: the k-slots of each 16-dim step
+        // are permuted so that a lane's K bytes are contiguous -- in half hf, k-step
+        // 4 hf + j takes dims 64 hf + 16 quad + 4 j .. + 3 for this lane's slots
+        // (2 quad, 2 quad + 1, 2 quad + 8, 2 quad + 9); q uses the same permutation.
+        uint32_t qa[8][2];
         float oacc[16][4];
+        // scores are q . k * scale (* the head's key scale for an FP8 cache), log2 units
+        const float sl2 = FP8 ? p.scale_log2 * p.k_scale[g] : p.scale_log2;
+        const float vsc = FP8 ? p.v_scale[g] : 1.f;
         float m_run = -INFINITY, l_run = 0.f, q_run = 0.f;
         int cur_b = 0;
 
@@ -259,8 +276,14 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks < nk && row_ok) {
                         const uint32_t *qr = reinterpret_cast<const uint32_t *>(qb + row * p.d);
-                        qa[ks][0] = qr[(ks * 16 + 2 * quad) >> 1];
-                        qa[ks][1] = qr[(ks * 16 + 8 + 2 * quad) >> 1];
+                        if constexpr (FP8) {
+                            const int d0 = (ks >> 2) * 64 + 16 * quad + 4 * (ks & 3);
+                            qa[ks][0] = bf16x2_to_f16x2(qr[d0 >> 1]);
+                            qa[ks][1] = bf16x2_to_f16x2(qr[(d0 + 2) >> 1]);
+                        } else {
+                            qa[ks][0] = qr[(ks * 16 + 2 * quad) >> 1];
+                            qa[ks][1] = qr[(ks * 16 + 8 + 2 * quad) >> 1];
+                        }
                     } else {
                         qa[ks][0] = 0u;
                         qa[ks][1] = 0u;
@@ -278,7 +301,26 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
             if (mt.ntok > 0) {
                 // ---- S = q K^T over the 16 tokens (two n-tiles of 8 tokens)
                 float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                {
+                if constexpr (FP8) {
+                    // token 8 nt + row: one 16-byte chunk per half holds this lane's dims
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const uint32_t rg = (uint32_t)(g * 16 + 8 * nt + row);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const uint4 w = lds128(kst + rg * 128u +
+                                                   (uint32_t)(((4 * hf + quad) ^ (int)(rg & 7u)) * 16));
+                            const uint32_t wj[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint32_t b0, b1;
+                                e4m3x4_to_f16x2x2(wj[j], b0, b1);
+                                mma_f16_16816(sacc[nt], qa[4 * hf + j][0], 0u, qa[4 * hf + j][1],
+                                              0u, b0, b1);
+                            }
+                        }
+                    }
+                } else {
                     const int mi = lane >> 3, i = lane & 7;
                     const int tok = (mi >> 1) * 8 + i;
                     const uint32_t r = (uint32_t)(g * 16 + tok);
@@ -298,10 +340,10 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 }
                 // ---- mask, online softmax (rows = query heads, 4 lanes per row)
                 float sv[4];
-                sv[0] = sacc[0][0] * p.scale_log2;
-                sv[1] = sacc[0][1] * p.scale_log2;
-                sv[2] = sacc[1][0] * p.scale_log2;
-                sv[3] = sacc[1][1] * p.scale_log2;
+                sv[0] = sacc[0][0] * sl2;
+                sv[1] = sacc[0][1] * sl2;
+                sv[2] = sacc[1][0] * sl2;
+                sv[3] = sacc[1][1] * sl2;
                 const int t0 = 2 * quad;
                 if (t0 >= mt.ntok || t0 < mt.lo) sv[0] = -INFINITY;
                 if (t0 + 1 >= mt.ntok || t0 + 1 < mt.lo) sv[1] = -INFINITY;
@@ -316,11 +358,12 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 float pr[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) pr[j] = ex2(sv[j] - m_use);
-                // P enters the PV product as bf16; O is normalised by the sum of the same
-                // rounded values, the log-sum-exp by the exact sum
-                const uint32_t pa0 = pack_bf16(pr[0], pr[1]);
-                const uint32_t pa2 = pack_bf16(pr[2], pr[3]);
-                float pq = (bf16lo(pa0) + bf16hi(pa0)) + (bf16lo(pa2) + bf16hi(pa2));
+                // P enters the PV product as bf16 (f16 for an FP8 cache); O is normalised
+                // by the sum of the same rounded values, the log-sum-exp by the exact sum
+                const uint32_t pa0 = FP8 ? pack_f16(pr[0], pr[1]) : pack_bf16(pr[0], pr[1]);
+                const uint32_t pa2 = FP8 ? pack_f16(pr[2], pr[3]) : pack_bf16(pr[2], pr[3]);
+                float pq = FP8 ? (f16lo(pa0) + f16hi(pa0)) + (f16lo(pa2) + f16hi(pa2))
+                               : (bf16lo(pa0) + bf16hi(pa0)) + (bf16lo(pa2) + bf16hi(pa2));
                 float ps = (pr[0] + pr[1]) + (pr[2] + pr[3]);
                 pq += __shfl_xor_sync(0xffffffffu, pq, 1);
                 ps += __shfl_xor_sync(0xffffffffu, ps, 1);
@@ -335,7 +378,35 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                     oacc[j][1] *= alpha;
                 }
                 // ---- O += P V
-                {
+                if constexpr (FP8) {
+                    // this lane's P covers tokens 2 quad, +1, +8, +9; its B column `row`
+                    // of n-tile dn is dim 16 row + dn, so each token row gives one
+                    // 16-byte chunk; bytes of two tokens are paired for the conversion
+                    const uint32_t ra = (uint32_t)(g * 16 + 2 * quad);
+                    const uint4 wa = lds128(vst + ra * 128u + (uint32_t)((row ^ (int)(ra & 7u)) * 16));
+                    const uint4 wb = lds128(vst + (ra + 1) * 128u +
+                                            (uint32_t)((row ^ (int)((ra + 1) & 7u)) * 16));
+                    const uint4 wc = lds128(vst + (ra + 8) * 128u +
+                                            (uint32_t)((row ^ (int)((ra + 8) & 7u)) * 16));
+                    const uint4 wd = lds128(vst + (ra + 9) * 128u +
+                                            (uint32_t)((row ^ (int)((ra + 9) & 7u)) * 16));
+                    const uint32_t a4[4] = {wa.x, wa.y, wa.z, wa.w}, b4[4] = {wb.x, wb.y, wb.z, wb.w};
+                    const uint32_t c4[4] = {wc.x, wc.y, wc.z, wc.w}, d4[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        uint32_t lo0, lo1, lo2, lo3, hi0, hi1, hi2, hi3;
+                        // (token 2q, token 2q+1) pairs of dims 4wi .. 4wi+3 -> b0 of 4 n-tiles
+                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x5140u), lo0, lo1);
+                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x7362u), lo2, lo3);
+                        // (token 2q+8, 2q+9) -> b1
+                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x5140u), hi0, hi1);
+                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x7362u), hi2, hi3);
+                        mma_f16_16816(oacc[4 * wi + 0], pa0, 0u, pa2, 0u, lo0, hi0);
+                        mma_f16_16816(oacc[4 * wi + 1], pa0, 0u, pa2, 0u, lo1, hi1);
+                        mma_f16_16816(oacc[4 * wi + 2], pa0, 0u, pa2, 0u, lo2, hi2);
+                        mma_f16_16816(oacc[4 * wi + 3], pa0, 0u, pa2, 0u, lo3, hi3);
+                    }
+                } else {
                     const int mi = lane >> 3, i = lane & 7;
                     const int tok = (mi & 1) * 8 + i;
                     const uint32_t r = (uint32_t)(g * 16 + tok);
@@ -361,13 +432,20 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 const long long slot = (long long)cur_b + blockIdx.x;
                 if (row_ok) {
                     const int h = g * Gq + row;
-                    const float inv = (q_run > 0.f) ? 1.f / q_run : 0.f;
+                    const float inv = (q_run > 0.f) ? vsc / q_run : 0.f;
                     float *po = p.part_o + (slot * p.Hq + h) * p.d;
 #pragma unroll
                     for (int dn = 0; dn < 16; ++dn) {
                         if (dn < nd) {
-                            *reinterpret_cast<float2 *>(po + dn * 8 + 2 * quad) =
-                                make_float2(oacc[dn][0] * inv, oacc[dn][1] * inv);
+                            if constexpr (FP8) {
+                                // logical columns 2 quad, 2 quad + 1 of n-tile dn are dims
+                                // 16 (2 quad) + dn and 16 (2 quad + 1) + dn
+                                po[32 * quad + dn] = oacc[dn][0] * inv;
+                                po[32 * quad + 16 + dn] = oacc[dn][1] * inv;
+                            } else {
+                                *reinterpret_cast<float2 *>(po + dn * 8 + 2 * quad) =
+                                    make_float2(oacc[dn][0] * inv, oacc[dn][1] * inv);
+                            }
                         }
                     }
                     if (quad == 0) {

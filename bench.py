@@ -165,6 +165,7 @@ KERNEL_SOURCES = {
     "prefill_tc_kernel": ("prefill_tc.cuh", "ptx.cuh"),
     "prefill_simt_kernel": ("prefill_simt.cuh", "ptx.cuh"),
     "decode_split_kernel": ("decode.cuh", "ptx.cuh"),
+    "decode_split_kernel<true>": ("decode.cuh", "ptx.cuh"),
 }
 
 
@@ -246,8 +247,10 @@ class Leg:
         w = inputs.make(name, batch)
         self.w = w
         self.scale = w.scale
-        if self.kind == "decode":
+        if self.kind in ("decode", "decode_fp8"):
             self.host = [w.q, w.k_cache, w.v_cache, w.page_table, w.seq_lens]
+            if self.kind == "decode_fp8":
+                self.host += [w.k_scale, w.v_scale]
             self.dev = [t.to(dev) for t in self.host]
             q, kc = self.dev[0], self.dev[1]
             B, Hq, d = w.q.shape
@@ -258,7 +261,7 @@ class Leg:
                                                                kc.shape[1]),
                                   dtype=torch.uint8, device=dev)
             self.work, self.unit, self.bound = decode_bytes(w), "GB/s", "hbm"
-            self.kernel = "decode_split_kernel"
+            self.kernel = "decode_split_kernel" + ("<true>" if self.kind == "decode_fp8" else "")
             self.shape = {"B": B, "Hq": Hq, "Hkv": int(kc.shape[2]), "d": d,
                           "page_size": int(kc.shape[1]),
                           "total_tokens": int(w.seq_lens.sum())}
@@ -296,6 +299,9 @@ class Leg:
         if self.kind == "decode":
             A.attn_decode_paged(d[0], d[1], d[2], d[3], d[4], self.scale, o=self.o, lse=self.lse,
                                 workspace=self.ws, stream=stream)
+        elif self.kind == "decode_fp8":
+            A.attn_decode_paged_fp8(d[0], d[1], d[2], d[5], d[6], d[3], d[4], self.scale,
+                                    o=self.o, lse=self.lse, workspace=self.ws, stream=stream)
         elif self.kind == "window":
             A.attn_fwd_window(d[0], d[1], d[2], self.w.window[0], self.w.window[1], self.scale,
                               o=self.o, lse=self.lse, stream=stream)
@@ -330,7 +336,7 @@ class Leg:
 
 
 def launches_per_call(leg) -> int:
-    return 2 if leg.kind == "decode" else 1
+    return 2 if leg.kind in ("decode", "decode_fp8") else 1
 
 
 def cpu_oracle_sample(w, kind: str, seconds: float, seed: int = 0):
@@ -342,6 +348,21 @@ def cpu_oracle_sample(w, kind: str, seconds: float, seed: int = 0):
     from oracle import oracle
     rng = np.random.default_rng(seed)
     work, done, t0 = 0.0, 0, time.perf_counter()
+    if kind == "decode_fp8":
+        args = (w.q.float().numpy(), w.k_cache.numpy(), w.v_cache.numpy(), w.k_scale.numpy(),
+                w.v_scale.numpy(), w.page_table.numpy(), w.seq_lens.numpy())
+        sl = w.seq_lens.numpy()
+        Hkv, d = w.k_cache.shape[2], w.k_cache.shape[3]
+        t0 = time.perf_counter()
+        while True:
+            b = int(rng.integers(0, len(sl)))
+            oracle.decode_paged_fp8(*args, w.scale, seqs=[b])
+            work += 2.0 * Hkv * d * 1.0 * float(sl[b])
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return work / el / 1e9, el, "%d random sequences (%.1f s, fp64)" % (done, el), \
+                    oracle.max_threads()
     if kind == "decode":
         arrs = [t.float().numpy() for t in (w.q, w.k_cache, w.v_cache)]
         pt, sl = w.page_table.numpy(), w.seq_lens.numpy()
@@ -413,7 +434,7 @@ def run_reference(args):
             vals.append(v)
             els += el
             descs.append(desc)
-        unit = "GB/s" if kind == "decode" else "TFLOP/s"
+        unit = "GB/s" if kind.startswith("decode") else "TFLOP/s"
         results.append((name, kind, float(np.mean(vals)), unit, els, descs[0], cores))
     name, kind, value, unit, els, desc, cores = results[0]
     line = {
@@ -553,7 +574,9 @@ def run_gpu(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sum(leg_ms) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if getattr(p0, "f32", False) else "bf16", "data": "synthetic",
+            "dtype": ("f32" if getattr(p0, "f32", False) else
+                      "f16 (E4M3 cache)" if p0.kind == "decode_fp8" else "bf16"),
+            "data": "synthetic",
             "config": config,
             "roofline": roofs[0],
             "e2e": e2e[0],
@@ -561,7 +584,7 @@ def run_gpu(args):
             "gpu_launches": args.steps * sum(launches_per_call(leg) for leg in legs),
             "clocks": clocks,
         }
-        line["%s_ms_per_step" % ("decode" if p0.kind == "decode" else "prefill")] = \
+        line["%s_ms_per_step" % ("decode" if p0.kind.startswith("decode") else "prefill")] = \
             leg_ms[0] / args.steps
         for i in range(1, nl):
             line[legs[i].kind] = {"value": leg_val[i], "unit": legs[i].unit,

@@ -158,6 +158,31 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_paged_fp8 -- attn_decode_paged against a cache held in 8-bit
+ * floating point (yapayzekasozluk.tr "attention" tag page, entry "KV Cache":
+ * keeping the cache in INT8/FP8 cuts its memory 2-4x at a small cost in
+ * quality).  The decode is bound by reading the cache, so halving its bytes
+ * roughly halves the time of a step.
+ *   k_cache,
+ *   v_cache     [num_pages, page_size, Hkv, d] uint8: FP8 E4M3 ("E4M3FN": bias 7,
+ *               no infinities, 0x7f/0xff NaN) bytes
+ *   k_scale,
+ *   v_scale     float32 [Hkv], DEVICE pointers: element c of head g of a cached key
+ *               (value) stands for k_scale[g] * e4m3 (v_scale[g] * e4m3)
+ *   q, o, lse, page_table, seq_lens, workspace and their rules as attn_decode_paged.
+ *   Inside the kernel the cache is widened to f16 (exactly) and q is rounded to
+ *   f16 (exact for |q| below 65504; larger values are not supported); scores and
+ *   sums are fp32.  Supported: d == 128, page_size == 16, Hkv <= 8, Hq/Hkv <= 8.
+ */
+attn_status_t attn_decode_paged_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                    const float *k_scale, const float *v_scale,
+                                    const int32_t *page_table, const int32_t *seq_lens, void *o,
+                                    float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                                    int num_pages, int max_pages_per_seq, float scale,
+                                    void *workspace, size_t workspace_bytes,
+                                    attn_stream_t stream);
+
+/*
  * attn_decode_paged_window -- attn_decode_paged where the new query attends only
  * to the last window + 1 cached tokens of its sequence (positions
  * seq_lens[b] - 1 - window .. seq_lens[b] - 1): the decode side of local
