@@ -40,7 +40,7 @@
 namespace attn07 {
 
 constexpr int kDecPage = 16;          // tokens per page (the kernel is built for it)
-constexpr int kDecMaxStages = 4;
+constexpr int kDecMaxStages = 8;
 constexpr int kDecMaxHkv = 8;
 
 struct DecodeParams {
@@ -67,6 +67,8 @@ struct DecodeStageMeta {
     int first;    // first page of a segment
     int last;     // last page of a segment
 };
+
+static_assert(sizeof(DecodeStageMeta) * kDecMaxStages <= 256, "stage metadata must fit");
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base):
 //   stage s:  bf16 cache: K half 0 .. K half (d/64 - 1), V half 0 .. V half (d/64 - 1),
@@ -129,11 +131,11 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
     const int nhalf = FP8 ? 1 : p.d / 64;   // TMA boxes per tensor and page
     const uint32_t ctrl = base + (uint32_t)S * stage_bytes;
     uint8_t *ctrl_ptr = base_ptr + (size_t)S * stage_bytes;
-    // control block: full[4] @0, empty[4] @32, meta[4] @64, scalars @192
-    const uint32_t full0 = ctrl, empty0 = ctrl + 32;
-    DecodeStageMeta *meta = reinterpret_cast<DecodeStageMeta *>(ctrl_ptr + 64);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl_ptr + 192);
-    int *shared_n = reinterpret_cast<int *>(ctrl_ptr + 196);
+    // control block: full[8] @0, empty[8] @64, meta[8] @128, scalars @384
+    const uint32_t full0 = ctrl, empty0 = ctrl + 64;
+    DecodeStageMeta *meta = reinterpret_cast<DecodeStageMeta *>(ctrl_ptr + 128);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl_ptr + 384);
+    int *shared_n = reinterpret_cast<int *>(ctrl_ptr + 388);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
