@@ -304,7 +304,9 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 // ---- S = q K^T over the 16 tokens (two n-tiles of 8 tokens)
                 float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 if constexpr (FP8) {
-                    // token 8 nt + row: one 16-byte chunk per half holds this lane's dims
+                    // token 8 nt + row: one 16-byte chunk per half holds this lane's dims;
+                    // odd k-steps accumulate apart (two shorter dependency chains)
+                    float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         const uint32_t rg = (uint32_t)(g * 16 + 8 * nt + row);
@@ -317,10 +319,12 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                             for (int j = 0; j < 4; ++j) {
                                 uint32_t b0, b1;
                                 e4m3x4_to_f16x2x2(wj[j], b0, b1);
-                                mma_f16_16816(sacc[nt], qa[4 * hf + j][0], 0u, qa[4 * hf + j][1],
-                                              0u, b0, b1);
+                                mma_f16_16816((j & 1) ? sodd[nt] : sacc[nt], qa[4 * hf + j][0], 0u,
+                                              qa[4 * hf + j][1], 0u, b0, b1);
                             }
                         }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
                     }
                 } else {
                     const int mi = lane >> 3, i = lane & 7;
@@ -374,16 +378,32 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 l_run = l_run * alpha + ps;   // exact sum -> log-sum-exp
                 q_run = q_run * alpha + pq;   // sum of the rounded P -> normalises O
                 m_run = m_new;
+                if constexpr (FP8) {
+                    // O^T tiles: columns are query heads 2 quad and 2 quad + 1, whose
+                    // factors live in lanes 8 quad and 8 quad + 4
+                    const float ae = __shfl_sync(0xffffffffu, alpha, 8 * quad);
+                    const float ao = __shfl_sync(0xffffffffu, alpha, 8 * quad + 4);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    oacc[j][0] *= alpha;
-                    oacc[j][1] *= alpha;
+                    for (int j = 0; j < 8; ++j) {
+                        oacc[j][0] *= ae;
+                        oacc[j][1] *= ao;
+                        oacc[j][2] *= ae;
+                        oacc[j][3] *= ao;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        oacc[j][0] *= alpha;
+                        oacc[j][1] *= alpha;
+                    }
                 }
                 // ---- O += P V
                 if constexpr (FP8) {
-                    // this lane's P covers tokens 2 quad, +1, +8, +9; its B column `row`
-                    // of n-tile dn is dim 16 row + dn, so each token row gives one
-                    // 16-byte chunk; bytes of two tokens are paired for the conversion
+                    // O^T += V^T P^T: M = 16 dims, N = 8 query heads, K = the 16 tokens.
+                    // This lane's P fragments (tokens 2 quad, +1, +8, +9 of head `row`) are
+                    // the B fragments as they stand.  M-tile mt's rows `row` and `row` + 8
+                    // are dims 16 row + 2 mt and 16 row + 2 mt + 1, so the lane's V bytes
+                    // are one 16-byte chunk per token; prmt pairs the bytes of two tokens.
                     const uint32_t ra = (uint32_t)(g * 16 + 2 * quad);
                     const uint4 wa = lds128(vst + ra * 128u + (uint32_t)((row ^ (int)(ra & 7u)) * 16));
                     const uint4 wb = lds128(vst + (ra + 1) * 128u +
@@ -396,17 +416,14 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                     const uint32_t c4[4] = {wc.x, wc.y, wc.z, wc.w}, d4[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
-                        uint32_t lo0, lo1, lo2, lo3, hi0, hi1, hi2, hi3;
-                        // (token 2q, token 2q+1) pairs of dims 4wi .. 4wi+3 -> b0 of 4 n-tiles
-                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x5140u), lo0, lo1);
-                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x7362u), lo2, lo3);
-                        // (token 2q+8, 2q+9) -> b1
-                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x5140u), hi0, hi1);
-                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x7362u), hi2, hi3);
-                        mma_f16_16816(oacc[4 * wi + 0], pa0, 0u, pa2, 0u, lo0, hi0);
-                        mma_f16_16816(oacc[4 * wi + 1], pa0, 0u, pa2, 0u, lo1, hi1);
-                        mma_f16_16816(oacc[4 * wi + 2], pa0, 0u, pa2, 0u, lo2, hi2);
-                        mma_f16_16816(oacc[4 * wi + 3], pa0, 0u, pa2, 0u, lo3, hi3);
+                        // m-tile 2 wi: bytes 0 (row) and 1 (row + 8); m-tile 2 wi + 1: bytes 2, 3
+                        uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
+                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x5140u), e0, e1);
+                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x5140u), e2, e3);
+                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x7362u), f0, f1);
+                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x7362u), f2, f3);
+                        mma_f16_16816(oacc[2 * wi], e0, e1, e2, e3, pa0, pa2);
+                        mma_f16_16816(oacc[2 * wi + 1], f0, f1, f2, f3, pa0, pa2);
                     }
                 } else {
                     const int mi = lane >> 3, i = lane & 7;
@@ -432,19 +449,33 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
             if (mt.last) {
                 // ---- partial result of this segment -> workspace slot b + cta
                 const long long slot = (long long)cur_b + blockIdx.x;
+                if constexpr (FP8) {
+                    // O^T: this lane holds heads 2 quad (c0, c2) and 2 quad + 1 (c1, c3)
+                    // at dims 16 row + 2 mt, + 1
+                    const float qe = __shfl_sync(0xffffffffu, q_run, 8 * quad);
+                    const float qo = __shfl_sync(0xffffffffu, q_run, 8 * quad + 4);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int hq = 2 * quad + hh;
+                        const float qr = hh ? qo : qe;
+                        if (hq < Gq) {
+                            const float inv = (qr > 0.f) ? vsc / qr : 0.f;
+                            float *po = p.part_o + (slot * p.Hq + g * Gq + hq) * p.d + 16 * row;
+#pragma unroll
+                            for (int mt = 0; mt < 8; ++mt)
+                                *reinterpret_cast<float2 *>(po + 2 * mt) =
+                                    make_float2(oacc[mt][hh] * inv, oacc[mt][2 + hh] * inv);
+                        }
+                    }
+                }
                 if (row_ok) {
                     const int h = g * Gq + row;
-                    const float inv = (q_run > 0.f) ? vsc / q_run : 0.f;
-                    float *po = p.part_o + (slot * p.Hq + h) * p.d;
+                    if constexpr (!FP8) {
+                        const float inv = (q_run > 0.f) ? vsc / q_run : 0.f;
+                        float *po = p.part_o + (slot * p.Hq + h) * p.d;
 #pragma unroll
-                    for (int dn = 0; dn < 16; ++dn) {
-                        if (dn < nd) {
-                            if constexpr (FP8) {
-                                // logical columns 2 quad, 2 quad + 1 of n-tile dn are dims
-                                // 16 (2 quad) + dn and 16 (2 quad + 1) + dn
-                                po[32 * quad + dn] = oacc[dn][0] * inv;
-                                po[32 * quad + 16 + dn] = oacc[dn][1] * inv;
-                            } else {
+                        for (int dn = 0; dn < 16; ++dn) {
+                            if (dn < nd) {
                                 *reinterpret_cast<float2 *>(po + dn * 8 + 2 * quad) =
                                     make_float2(oacc[dn][0] * inv, oacc[dn][1] * inv);
                             }
