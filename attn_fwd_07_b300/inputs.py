@@ -35,7 +35,7 @@ import torch
 
 BLOCK = 1 << 22
 
-TAG_Q, TAG_K, TAG_V, TAG_LEN, TAG_PERM = 1, 2, 3, 4, 5
+TAG_Q, TAG_K, TAG_V, TAG_LEN, TAG_PERM, TAG_QCHUNK = 1, 2, 3, 4, 5, 6
 
 
 def _threads() -> int:
@@ -177,6 +177,40 @@ def paged(lens, Hq, Hkv, d, seed, page_size=16, max_pages=None, dtype=torch.bflo
 
 
 @dataclass
+class ChunkPaged:
+    q: torch.Tensor           # [Tq, Hq, d] bf16: each sequence's chunk of new queries
+    k_cache: torch.Tensor     # [P, page_size, Hkv, d] bf16
+    v_cache: torch.Tensor
+    page_table: torch.Tensor  # int32 [B, maxp]
+    seq_lens: torch.Tensor    # int32 [B]: cached tokens, the chunk's own included
+    cu_seqlens_q: torch.Tensor  # int32 [B + 1]
+    causal: bool
+    scale: float
+
+    @property
+    def q_lens(self):
+        cu = self.cu_seqlens_q.numpy()
+        return (cu[1:] - cu[:-1]).astype(np.int64)
+
+
+def chunked(ctx_lens, q_lens, Hq, Hkv, d, seed, page_size=16, factor=1.0, causal=True,
+            scale=None) -> ChunkPaged:
+    """Paged caches of ctx_lens tokens (the paged recipe) and, per sequence, a chunk of
+    q_lens new queries packed along the token axis (the chunk's tokens are the last
+    q_len of the cache)."""
+    ctx = np.asarray(ctx_lens, np.int64)
+    ql = np.asarray(q_lens, np.int64)
+    assert (ql <= ctx).all() and (ql >= 0).all()
+    cache = paged(ctx, Hq, Hkv, d, seed, page_size=page_size, factor=factor)
+    cu = np.zeros(len(ql) + 1, np.int32)
+    cu[1:] = np.cumsum(ql)
+    q = normal_tensor((int(cu[-1]), Hq, d), seed, TAG_QCHUNK, torch.bfloat16, factor)
+    return ChunkPaged(q, cache.k_cache, cache.v_cache, cache.page_table, cache.seq_lens,
+                      torch.from_numpy(cu), causal,
+                      (1.0 / math.sqrt(d)) if scale is None else scale)
+
+
+@dataclass
 class PagedFP8:
     q: torch.Tensor           # [B, Hq, d] bf16
     k_cache: torch.Tensor     # [P, page_size, Hkv, d] uint8 (FP8 E4M3 bytes)
@@ -268,6 +302,15 @@ WORKLOADS = {
         dict(B=64, lo=1024, hi=32768, Hq=32, Hkv=8, d=128, page_size=16, factor=1.0),
         "B=64 one query each, lengths U[1024,32768], Hq=32 Hkv=8 d=128, 16-token pages, "
         "permuted page table, N(0,1) cache quantised to FP8 E4M3 with per-head scales"),
+    # chunked prefill with prefix caching: 8 sequences whose cached prefixes are
+    # U[1024, 16384] tokens each receive a chunk of 2048 new tokens, which attend
+    # causally to the prefix and to themselves through the page table
+    "chunked_prefill_b8": Workload(
+        "chunked_prefill_b8", "chunk", 7,
+        dict(B=8, lo=1024, hi=16384, chunk=2048, Hq=32, Hkv=8, d=128, page_size=16,
+             factor=1.0),
+        "8 sequences, cached prefixes U[1024,16384] + a 2048-token chunk each, Hq=32 Hkv=8 "
+        "d=128, 16-token pages, permuted page table, bf16 N(0,1), causal"),
     "decode_paged_b64": Workload(
         "decode_paged_b64", "decode", 5,
         dict(B=64, lo=1024, hi=32768, Hq=32, Hkv=8, d=128, page_size=16,
@@ -305,6 +348,12 @@ def make(name: str, batch: int | None = None):
         maxp = (p["hi"] + p["page_size"] - 1) // p["page_size"]
         return paged(lens, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"], maxp, p["dtype"],
                      p["factor"])
+    if w.kind == "chunk":
+        B = p["B"] if batch is None else int(batch)
+        prefix = lengths(B, p["lo"], p["hi"], w.seed)
+        ql = np.full(B, p["chunk"], np.int64)
+        return chunked(prefix + ql, ql, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"],
+                       p["factor"])
     if w.kind == "decode_fp8":
         B = p["B"] if batch is None else int(batch)
         lens = lengths(B, p["lo"], p["hi"], w.seed)

@@ -427,6 +427,79 @@ int oracle_decode_paged_window_rows(const float *q, const float *k_cache, const 
 }
 
 /*
+ * A chunk of new queries against a paged cache (prefix caching / chunked
+ * prefill; yapayzekasozluk.tr "attention" tag page, entry "KV Cache": the keys
+ * and values of earlier tokens, and of a reused prompt prefix, are kept and
+ * the new tokens attend to them).  Sequence s has seq_lens[s] cached tokens,
+ * the last q_len of which are the chunk's own tokens (the caller appended
+ * them to the cache before the call); its queries are rows cu_q[s] ..
+ * cu_q[s+1]-1 of q, query i sitting at position seq_lens[s] - q_len + i.
+ * Causal: query i sees the cached tokens at positions <= its own; otherwise
+ * all seq_lens[s] of them.  Page lookup as oracle_decode_paged_rows.
+ * q [Tq, Hq, d]; rows lists (token t of q, head h) pairs; o_rows [n, d],
+ * lse_rows [n].  Returns 0, or -1 on a bad argument or page id.
+ */
+int oracle_chunk_paged_rows(const float *q, const float *k_cache, const float *v_cache,
+                            const int32_t *page_table, const int32_t *seq_lens,
+                            const int32_t *cu_q, int num_seqs, int total_q, int Hq, int Hkv,
+                            int d, int page_size, int num_pages, int maxp, int causal,
+                            double scale, const int32_t *rows, int64_t nrows,
+                            double *o_rows, double *lse_rows, int nthreads)
+{
+    if (num_seqs < 0 || total_q < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 ||
+        page_size <= 0)
+        return -1;
+    if (cu_q[0] != 0 || cu_q[num_seqs] != total_q) return -1;
+    int64_t maxlen = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        const int64_t qlen = (int64_t)cu_q[s + 1] - cu_q[s];
+        const int64_t len = seq_lens[s];
+        if (qlen < 0 || len < qlen || len > (int64_t)maxp * page_size) return -1;
+        for (int64_t p = 0; p < (len + page_size - 1) / page_size; ++p) {
+            const int32_t pid = page_table[(int64_t)s * maxp + p];
+            if (pid < 0 || pid >= num_pages) return -1;
+        }
+        if (len > maxlen) maxlen = len;
+    }
+    const int group = Hq / Hkv;
+    const int nt = set_threads(nthreads);
+    int bad = 0;
+#pragma omp parallel num_threads(nt) reduction(| : bad)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(maxlen > 0 ? maxlen : 1));
+        const float **kr = (const float **)malloc(sizeof(float *) * (size_t)(maxlen > 0 ? maxlen : 1));
+        const float **vr = (const float **)malloc(sizeof(float *) * (size_t)(maxlen > 0 ? maxlen : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            const int t = rows[2 * r], h = rows[2 * r + 1];
+            if (t < 0 || t >= total_q || h < 0 || h >= Hq) {
+                bad = 1;
+                continue;
+            }
+            int sq = 0;
+            while (cu_q[sq + 1] <= t) ++sq;
+            const int64_t qlen = (int64_t)cu_q[sq + 1] - cu_q[sq];
+            const int64_t len = seq_lens[sq];
+            const int64_t pos = len - qlen + (t - cu_q[sq]);
+            const int64_t n = causal ? pos + 1 : len;
+            const int g = h / group;
+            for (int64_t j = 0; j < n; ++j) {
+                const int64_t page = page_table[(int64_t)sq * maxp + j / page_size];
+                const int64_t off = ((page * page_size + j % page_size) * Hkv + g) * d;
+                kr[j] = k_cache + off;
+                vr[j] = v_cache + off;
+            }
+            attention_row(q + ((int64_t)t * Hq + h) * d, kr, vr, n, d, scale, s,
+                          o_rows + r * d, lse_rows + r);
+        }
+        free(s);
+        free(kr);
+        free(vr);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
  * The value of one FP8 E4M3 byte (OCP 8-bit floating point, "E4M3FN": 1 sign
  * bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities; exponent
  * and mantissa all ones is NaN):

@@ -60,6 +60,8 @@ def _load():
         lib.oracle_e4m3_value.restype = D
         lib.oracle_decode_paged_fp8_rows.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, D,
                                                      P, I, P, P, I]
+        lib.oracle_chunk_paged_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
+                                                D, P, I64, P, P, I]
         lib.oracle_online_softmax_stats.argtypes = [P, I64, I64, P, P]
         lib.oracle_online_softmax_stats.restype = None
         lib.oracle_merge_parts.argtypes = [P, P, I, I, P, P]
@@ -67,7 +69,7 @@ def _load():
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_attn_varlen",
                      "oracle_attn_window_rows", "oracle_decode_paged_window_rows",
-                     "oracle_decode_paged_fp8_rows",
+                     "oracle_decode_paged_fp8_rows", "oracle_chunk_paged_rows",
                      "oracle_decode_paged_rows", "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -218,6 +220,34 @@ def decode_paged_window(q, k_cache, v_cache, page_table, seq_lens, window: int, 
                                                  _p(seqs), n, _p(o), _p(lse), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_decode_paged_window_rows rejected its arguments")
+    return o, lse
+
+
+def chunk_paged_rows(q, k_cache, v_cache, page_table, seq_lens, cu_seqlens_q, causal: bool,
+                     scale: float, rows=None, nthreads: int = 0):
+    """A chunk of queries per sequence against its paged cache: q [Tq,Hq,d] packed by
+    cu_seqlens_q; sequence s has seq_lens[s] cached tokens, the last q_len of them the
+    chunk's own, so query i sits at position seq_lens[s] - q_len + i (causal: it sees
+    positions <= its own).  rows: [n, 2] (token, head) pairs, default all ->
+    (o [n, d], lse [n])."""
+    q, kc, vc = _f32(q), _f32(k_cache), _f32(v_cache)
+    pt, sl, cu = _i32(page_table), _i32(seq_lens), _i32(cu_seqlens_q)
+    Tq, Hq, d = q.shape
+    P, ps, Hkv, _ = kc.shape
+    maxp = pt.shape[1]
+    if rows is None:
+        t, h = np.meshgrid(np.arange(Tq), np.arange(Hq), indexing="ij")
+        rows = np.stack([t.ravel(), h.ravel()], 1)
+    rows = _i32(rows).reshape(-1, 2)
+    n = rows.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.zeros((n,), np.float64)
+    rc = _load().oracle_chunk_paged_rows(_p(q), _p(kc), _p(vc), _p(pt), _p(sl), _p(cu),
+                                         len(cu) - 1, Tq, Hq, Hkv, d, ps, P, maxp,
+                                         int(bool(causal)), float(scale), _p(rows), n, _p(o),
+                                         _p(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_chunk_paged_rows rejected its arguments")
     return o, lse
 
 
