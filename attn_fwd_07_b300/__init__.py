@@ -16,7 +16,8 @@ import os
 import torch
 
 __all__ = [
-    "AttnError", "load_library", "attn_fwd", "attn_fwd_window", "attn_fwd_f32",
+    "AttnError", "load_library", "attn_fwd", "attn_fwd_window", "attn_fwd_chunked_paged",
+    "attn_fwd_f32",
     "attn_fwd_varlen", "attn_decode_paged", "attn_decode_paged_window", "attn_decode_paged_fp8",
     "attn_decode_paged_noalloc", "attn_decode_workspace_size", "attn_status_string",
     "attn_get_device_status", "attn_version", "attn_last_cuda_error",
@@ -58,6 +59,8 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]
+        lib.attn_fwd_chunked_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I,
+                                               I, I, F, P]
         lib.attn_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
                                               P, SZ, P]
         lib.attn_decode_paged_window.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
@@ -75,6 +78,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_last_cuda_error.restype = ctypes.c_char_p
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
                      "attn_fwd_window", "attn_decode_paged_window", "attn_decode_paged_fp8",
+                     "attn_fwd_chunked_paged",
                      "attn_decode_paged_noalloc", "attn_get_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -204,6 +208,34 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = True,
                                         int(max_seqlen), Hq, Hkv, d, int(bool(causal)),
                                         float(scale), _stream(stream))
     _check(rc, "attn_fwd_varlen")
+    return o, lse
+
+
+def attn_fwd_chunked_paged(q, k_cache, v_cache, page_table, seq_lens, cu_seqlens_q,
+                           max_qlen: int, causal: bool = True, scale: float | None = None,
+                           o=None, lse=None, want_lse: bool = True, stream=None):
+    """A chunk of queries per sequence against its paged cache.  q [Tq,Hq,d] packed by
+    cu_seqlens_q (int32 [S+1], device); caches [P,16,Hkv,d]; page_table int32 [S,maxp];
+    seq_lens int32 [S] (device, the chunk's own tokens included)
+    -> (o [Tq,Hq,d] bf16, lse [Hq,Tq] fp32)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"),
+                 (cu_seqlens_q, "cu_seqlens_q")):
+        _need(t, torch.int32, n)
+    Tq, Hq, d = q.shape
+    P, ps, Hkv, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_fwd_chunked_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens),
+        _ptr(cu_seqlens_q), _ptr(o), _ptr(lse), cu_seqlens_q.numel() - 1, Tq, int(max_qlen), Hq,
+        Hkv, d, ps, P, page_table.shape[1], int(bool(causal)), float(scale), _stream(stream))
+    _check(rc, "attn_fwd_chunked_paged")
     return o, lse
 
 

@@ -77,11 +77,16 @@ attn_status_t device_state(DeviceState **out) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)prefill_simt_smem_bytes(kSimtMaxD))) != cudaSuccess)
             return cuda_fail(e);
-        if ((e = cudaFuncSetAttribute(prefill_tc_kernel<128>,
+        if ((e = cudaFuncSetAttribute(prefill_tc_kernel<128, false>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)PrefillCfg<128>::SMEM)) != cudaSuccess)
-            return cuda_fail(e);
-        if ((e = cudaFuncSetAttribute(prefill_tc_kernel<64>,
+                                      (int)PrefillCfg<128>::SMEM)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prefill_tc_kernel<128, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)PrefillCfg<128>::SMEM)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prefill_tc_kernel<64, false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)PrefillCfg<64>::SMEM)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prefill_tc_kernel<64, true>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)PrefillCfg<64>::SMEM)) != cudaSuccess)
             return cuda_fail(e);
@@ -121,12 +126,22 @@ attn_status_t make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Launch the tensor-core prefill on a [tokens, heads, d] layout with
-// `nbatch` sequences along the outermost axis (dense) or one packed axis (varlen).
+// Keys and values held in a cache of 16-token pages (chunked prefill).
+struct PagedKV {
+    const int32_t *page_table;  // [nseq, maxp]
+    const int32_t *kv_lens;     // [nseq]
+    int maxp, num_pages;
+};
+
+// Launch the tensor-core prefill on a [tokens, heads, d] layout with `nseq`
+// sequences along the outermost axis (dense) or one packed axis (varlen,
+// cu_seqlens non-null).  With `paged`, q is a packed chunk per sequence and k, v
+// are caches [num_pages, 16, Hkv, d] read through the page table.
 attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, void *o, float *lse,
                                 const int32_t *cu_seqlens, int nseq, int N_or_total,
                                 int ntiles, int Hq, int Hkv, int d, int wl, int wr,
-                                float scale, cudaStream_t stream) {
+                                float scale, cudaStream_t stream,
+                                const PagedKV *paged = nullptr) {
     DeviceState *st = nullptr;
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
@@ -142,8 +157,19 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     const cuuint32_t box[4] = {64, 1, 128, 1};
     CUtensorMap mq, mk, mv;
     if ((s = make_map(&mq, q, 4, dq, sq, box)) != ATTN_OK) return s;
-    if ((s = make_map(&mk, k, 4, dk, sk, box)) != ATTN_OK) return s;
-    if ((s = make_map(&mv, v, 4, dk, sk, box)) != ATTN_OK) return s;
+    if (paged) {
+        // cache as (dim, token-in-page, head, page); one box = one page of one head
+        const cuuint64_t dc[4] = {(cuuint64_t)d, 16, (cuuint64_t)Hkv,
+                                  (cuuint64_t)paged->num_pages};
+        const cuuint64_t sc[3] = {(cuuint64_t)Hkv * d * 2, (cuuint64_t)d * 2,
+                                  (cuuint64_t)16 * Hkv * d * 2};
+        const cuuint32_t bc[4] = {64, 16, 1, 1};
+        if ((s = make_map(&mk, k, 4, dc, sc, bc)) != ATTN_OK) return s;
+        if ((s = make_map(&mv, v, 4, dc, sc, bc)) != ATTN_OK) return s;
+    } else {
+        if ((s = make_map(&mk, k, 4, dk, sk, box)) != ATTN_OK) return s;
+        if ((s = make_map(&mv, v, 4, dk, sk, box)) != ATTN_OK) return s;
+    }
     PrefillParams p;
     p.o = static_cast<__nv_bfloat16 *>(o);
     p.lse = lse;
@@ -161,16 +187,29 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     p.wl = wl < 0 ? -1 : wl;
     p.wr = wr < 0 ? -1 : wr;
     p.scale_log2 = scale * kLog2e;
+    p.page_table = paged ? paged->page_table : nullptr;
+    p.kv_lens = paged ? paged->kv_lens : nullptr;
+    p.maxp = paged ? paged->maxp : 0;
+    p.num_pages = paged ? paged->num_pages : 0;
     const long long grid = p.head_pairs ? (long long)ntiles * (Hq / 2) * nseq
                                         : (long long)((ntiles + 1) / 2) * Hq * nseq;
     if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     if (grid == 0) return ATTN_OK;
+    const unsigned gx = (unsigned)grid;
     if (d == 128) {
-        prefill_tc_kernel<128><<<(unsigned)grid, PrefillCfg<128>::THREADS, PrefillCfg<128>::SMEM,
-                                 stream>>>(p, mq, mk, mv);
+        if (paged)
+            prefill_tc_kernel<128, true><<<gx, PrefillCfg<128>::THREADS, PrefillCfg<128>::SMEM,
+                                           stream>>>(p, mq, mk, mv);
+        else
+            prefill_tc_kernel<128, false><<<gx, PrefillCfg<128>::THREADS, PrefillCfg<128>::SMEM,
+                                            stream>>>(p, mq, mk, mv);
     } else {
-        prefill_tc_kernel<64><<<(unsigned)grid, PrefillCfg<64>::THREADS, PrefillCfg<64>::SMEM,
-                                stream>>>(p, mq, mk, mv);
+        if (paged)
+            prefill_tc_kernel<64, true><<<gx, PrefillCfg<64>::THREADS, PrefillCfg<64>::SMEM,
+                                          stream>>>(p, mq, mk, mv);
+        else
+            prefill_tc_kernel<64, false><<<gx, PrefillCfg<64>::THREADS, PrefillCfg<64>::SMEM,
+                                           stream>>>(p, mq, mk, mv);
     }
     return launch_status();
 }
@@ -257,6 +296,29 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     const int ntiles = (max_seqlen + 127) / 128;
     return launch_prefill_tc(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, ntiles, Hq, Hkv,
                              d, -1, causal ? 0 : -1, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_chunked_paged(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *page_table, const int32_t *seq_lens,
+                                     const int32_t *cu_seqlens_q, void *o, float *lse,
+                                     int num_seqs, int total_q, int max_qlen, int Hq, int Hkv,
+                                     int d, int page_size, int num_pages, int max_pages_per_seq,
+                                     int causal, float scale, attn_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !cu_seqlens_q || !o)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || total_q < 0 || max_qlen < 0 || Hq <= 0 || Hkv <= 0 ||
+        Hq % Hkv != 0 || d <= 0 || page_size <= 0 || num_pages <= 0 || max_pages_per_seq <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+        return ATTN_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || page_size != 16) return ATTN_ERR_UNSUPPORTED;
+    if (total_q == 0 || max_qlen == 0) return ATTN_OK;
+    const int ntiles = (max_qlen + 127) / 128;
+    const PagedKV pk{page_table, seq_lens, max_pages_per_seq, num_pages};
+    return launch_prefill_tc(q, k_cache, v_cache, o, lse, cu_seqlens_q, num_seqs, total_q,
+                             ntiles, Hq, Hkv, d, -1, causal ? 0 : -1, scale,
+                             reinterpret_cast<cudaStream_t>(stream), &pk);
 }
 
 attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,

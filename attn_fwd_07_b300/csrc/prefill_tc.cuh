@@ -68,6 +68,11 @@ struct PrefillParams {
     int wl, wr;     // query i sees keys i - wl .. i + wr; -1: no limit on that side
                     // (causal: wl = -1, wr = 0; full: wl = wr = -1)
     float scale_log2;
+    // paged keys/values (a chunk of queries against a cache): sequence s has
+    // kv_lens[s] cached tokens, its chunk is the last q_len of them
+    const int32_t *page_table;  // [nseq, maxp]
+    const int32_t *kv_lens;     // [nseq]
+    int maxp, num_pages;
 };
 
 template <int D>
@@ -104,7 +109,11 @@ enum : uint32_t {
     BAR_COUNT = 24
 };
 
-template <int D>
+// PAGED: keys and values come from a cache of 16-token pages through the page
+// table (eight page boxes per 128-key tile, assembled into the same shared-memory
+// layout), queries are a packed chunk per sequence positioned at the end of the
+// sequence's cached tokens.
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(384, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -120,15 +129,26 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     const int rem = (int)(blockIdx.x % units);
     const int hu = rem % hunits;
     const int sq = rem / hunits;
-    int tok0, len, batch;
+    // query rows [0, qlen) of this sequence sit at positions qoff + i; keys at [0, kvlen)
+    int tok0, qlen, batch;
     if (p.cu_seqlens) {
         tok0 = p.cu_seqlens[sq];
-        len = p.cu_seqlens[sq + 1] - tok0;
+        qlen = p.cu_seqlens[sq + 1] - tok0;
         batch = 0;
     } else {
         tok0 = 0;
-        len = p.N;
+        qlen = p.N;
         batch = sq;
+    }
+    int kvlen = qlen, qoff = 0;
+    if constexpr (PAGED) {
+        kvlen = p.kv_lens[sq];
+        qoff = kvlen - qlen;
+        if (qoff < 0 || kvlen > p.maxp * 16) {  // uniform: the sequence's sizes are invalid
+            if (threadIdx.x == 0 && outer == nouter - 1 && qlen > 0)
+                record_status(p.status, kStatusBounds);
+            return;
+        }
     }
     // the CTA's two tiles: query head, first row, and the key tiles [jlo, jhi] each needs
     int head[2], row0[2], jlo[2], jhi[2];
@@ -145,10 +165,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     bool valid[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        valid[t] = outer >= 0 && row0[t] < len;
-        const int last_row = min(row0[t] + C::BM, len) - 1;
-        const int lo_key = p.wl < 0 ? 0 : max(0, row0[t] - p.wl);
-        const int hi_key = p.wr < 0 ? len - 1 : min(len - 1, last_row + p.wr);
+        valid[t] = outer >= 0 && row0[t] < qlen;
+        const int last_row = min(row0[t] + C::BM, qlen) - 1;
+        const int lo_key = p.wl < 0 ? 0 : max(0, qoff + row0[t] - p.wl);
+        const int hi_key = p.wr < 0 ? kvlen - 1 : min(kvlen - 1, qoff + last_row + p.wr);
         jlo[t] = lo_key / C::BN;
         jhi[t] = hi_key / C::BN;
     }
@@ -222,17 +242,46 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                                 hf * 64, head[t], tok0 + row0[t], batch, pol_q);
             }
             int issued_k = 0, issued_v = 0;
+            const int npg = (kvlen + 15) / 16;  // pages holding this sequence's keys
             for (int j = 0; j < n_kv; ++j) {
                 const int kvrow = tok0 + (J0 + j) * C::BN;
+                // PAGED: the tile's eight 16-token pages; a page past the sequence, or a
+                // page id out of range (reported), is loaded from an out-of-range page
+                // coordinate, which the copy fills with zeros
+                int pcoord[8];
+                if constexpr (PAGED) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
+                        const int pg = (J0 + j) * 8 + q8;
+                        int pid = p.num_pages;
+                        if (pg < npg) {
+                            pid = p.page_table[(long long)sq * p.maxp + pg];
+                            if ((unsigned)pid >= (unsigned)p.num_pages) {
+                                record_status(p.status, kStatusBounds);
+                                pid = p.num_pages;
+                            }
+                        }
+                        pcoord[q8] = pid;
+                    }
+                }
                 const int sk = j % C::SK;
                 if (!mbar_wait(bar(BAR_KEMPTY + sk), ((uint32_t)(j / C::SK) & 1u) ^ 1u, p.status,
                                abort_flag))
                     break;
                 mbar_arrive_expect_tx(bar(BAR_KFULL + sk), C::TILE);
 #pragma unroll
-                for (int hf = 0; hf < C::NH; ++hf)
-                    tma_load_4d(base + C::OFF_K + sk * C::TILE + hf * C::HALF, &tmK,
-                                bar(BAR_KFULL + sk), hf * 64, g, kvrow, batch, pol_kv);
+                for (int hf = 0; hf < C::NH; ++hf) {
+                    const uint32_t dst = base + C::OFF_K + sk * C::TILE + hf * C::HALF;
+                    if constexpr (PAGED) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 8; ++q8)
+                            tma_load_4d(dst + q8 * 2048u, &tmK, bar(BAR_KFULL + sk), hf * 64, 0,
+                                        g, pcoord[q8], pol_kv);
+                    } else {
+                        tma_load_4d(dst, &tmK, bar(BAR_KFULL + sk), hf * 64, g, kvrow, batch,
+                                    pol_kv);
+                    }
+                }
                 issued_k = j + 1;
                 const int sv = j % C::SV;
                 if (!mbar_wait(bar(BAR_VEMPTY + sv), ((uint32_t)(j / C::SV) & 1u) ^ 1u, p.status,
@@ -240,9 +289,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     break;
                 mbar_arrive_expect_tx(bar(BAR_VFULL + sv), C::TILE);
 #pragma unroll
-                for (int hf = 0; hf < C::NH; ++hf)
-                    tma_load_4d(base + C::OFF_V + sv * C::TILE + hf * C::HALF, &tmV,
-                                bar(BAR_VFULL + sv), hf * 64, g, kvrow, batch, pol_kv);
+                for (int hf = 0; hf < C::NH; ++hf) {
+                    const uint32_t dst = base + C::OFF_V + sv * C::TILE + hf * C::HALF;
+                    if constexpr (PAGED) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 8; ++q8)
+                            tma_load_4d(dst + q8 * 2048u, &tmV, bar(BAR_VFULL + sv), hf * 64, 0,
+                                        g, pcoord[q8], pol_kv);
+                    } else {
+                        tma_load_4d(dst, &tmV, bar(BAR_VFULL + sv), hf * 64, g, kvrow, batch,
+                                    pol_kv);
+                    }
+                }
                 issued_v = j + 1;
             }
             if (*abort_flag) {
@@ -350,8 +408,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         const uint32_t ocol = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
         const int qpos = (t ? row0[1] : row0[0]) + r;  // position within the sequence
         // allowed keys of this row: [klo, khi]
-        const int klo = p.wl < 0 ? 0 : qpos - p.wl;
-        const int khi = p.wr < 0 ? len - 1 : min(len - 1, qpos + p.wr);
+        const int klo = p.wl < 0 ? 0 : qoff + qpos - p.wl;
+        const int khi = p.wr < 0 ? kvlen - 1 : min(kvlen - 1, qoff + qpos + p.wr);
         float m_ref = -INFINITY;                   // log2 units, scaled
         float l = 0.f;                             // sum of P (fp32) -> LSE
         float lr = 0.f;                            // sum of bf16-rounded P -> normalises O
@@ -452,7 +510,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-                const bool row_ok = qpos < len;
+                const bool row_ok = qpos < qlen;
                 const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
                 const int h = t ? head[1] : head[0];
                 const long long tok = (long long)tok0 + qpos;

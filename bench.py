@@ -204,6 +204,16 @@ def prefill_flops(w) -> float:
     """Algorithmic FLOPs of one prefill: 4*d per (query, key) pair (QK^T and PV, 2*d
     each) over N^2 pairs per sequence and head, halved when causal (2*B*Hq*N^2*d); a
     sliding window counts its allowed pairs exactly."""
+    if hasattr(w, "cu_seqlens_q"):
+        # a chunk per sequence: query i of q_len sees positions <= ctx - q_len + i
+        _, Hq, d = w.q.shape
+        ctx = w.seq_lens.numpy().astype(np.float64)
+        ql = w.q_lens.astype(np.float64)
+        if w.causal:
+            pairs = float((ql * (ctx - ql) + ql * (ql + 1) / 2.0).sum())
+        else:
+            pairs = float((ql * ctx).sum())
+        return 4.0 * Hq * d * pairs
     if getattr(w, "window", None) is not None:
         # a sliding window: the exact number of allowed (query, key) pairs
         B, N, Hq, d = w.q.shape
@@ -266,11 +276,21 @@ class Leg:
                           "page_size": int(kc.shape[1]),
                           "total_tokens": int(w.seq_lens.sum())}
         else:
-            self.host = [w.q, w.k, w.v] + ([w.cu_seqlens] if self.kind == "varlen" else [])
+            if self.kind == "chunk":
+                self.host = [w.q, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.cu_seqlens_q]
+            else:
+                self.host = [w.q, w.k, w.v] + ([w.cu_seqlens] if self.kind == "varlen" else [])
             self.dev = [t.to(dev) for t in self.host]
             q = self.dev[0]
             self.o = torch.empty_like(q)
-            if self.kind == "window":
+            if self.kind == "chunk":
+                T, Hq, d = w.q.shape
+                self.max_len = int(w.q_lens.max())
+                self.lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+                self.shape = {"seqs": len(w.q_lens), "total_q": T,
+                              "cached_tokens": int(w.seq_lens.sum()), "Hq": Hq,
+                              "Hkv": int(w.k_cache.shape[2]), "d": d, "causal": w.causal}
+            elif self.kind == "window":
                 B, N, Hq, d = w.q.shape
                 self.lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
                 self.shape = {"B": B, "N": N, "Hq": Hq, "Hkv": int(w.k.shape[2]), "d": d,
@@ -302,6 +322,10 @@ class Leg:
         elif self.kind == "decode_fp8":
             A.attn_decode_paged_fp8(d[0], d[1], d[2], d[5], d[6], d[3], d[4], self.scale,
                                     o=self.o, lse=self.lse, workspace=self.ws, stream=stream)
+        elif self.kind == "chunk":
+            A.attn_fwd_chunked_paged(d[0], d[1], d[2], d[3], d[4], d[5], self.max_len,
+                                     self.w.causal, self.scale, o=self.o, lse=self.lse,
+                                     stream=stream)
         elif self.kind == "window":
             A.attn_fwd_window(d[0], d[1], d[2], self.w.window[0], self.w.window[1], self.scale,
                               o=self.o, lse=self.lse, stream=stream)
@@ -348,6 +372,27 @@ def cpu_oracle_sample(w, kind: str, seconds: float, seed: int = 0):
     from oracle import oracle
     rng = np.random.default_rng(seed)
     work, done, t0 = 0.0, 0, time.perf_counter()
+    if kind == "chunk":
+        args = (w.q.float().numpy(), w.k_cache.float().numpy(), w.v_cache.float().numpy(),
+                w.page_table.numpy(), w.seq_lens.numpy(), w.cu_seqlens_q.numpy(), w.causal,
+                w.scale)
+        cu, ctx = w.cu_seqlens_q.numpy(), w.seq_lens.numpy()
+        Tq, Hq, d = w.q.shape
+        n_rows = 256
+        t0 = time.perf_counter()
+        while True:
+            t = rng.integers(0, Tq, n_rows)
+            rows = np.stack([t, rng.integers(0, Hq, n_rows)], 1)
+            oracle.chunk_paged_rows(*args, rows=rows)
+            sq = np.searchsorted(cu, t, side="right") - 1
+            pos = ctx[sq] - (cu[sq + 1] - cu[sq]) + (t - cu[sq])
+            keys = (pos + 1.0) if w.causal else ctx[sq].astype(np.float64)
+            work += float(4.0 * d * keys.sum())
+            done += n_rows
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return work / el / 1e12, el, "%d random query rows (%.1f s, fp64)" % (done, el), \
+                    oracle.max_threads()
     if kind == "decode_fp8":
         args = (w.q.float().numpy(), w.k_cache.numpy(), w.v_cache.numpy(), w.k_scale.numpy(),
                 w.v_scale.numpy(), w.page_table.numpy(), w.seq_lens.numpy())

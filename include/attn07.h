@@ -99,6 +99,39 @@ attn_status_t attn_fwd_window(const void *q, const void *k, const void *v, void 
                               int window_right, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_chunked_paged -- a chunk of new queries per sequence against that
+ * sequence's paged key/value cache: chunked prefill, and prefill after a reused
+ * (cached) prompt prefix (yapayzekasozluk.tr "attention" tag page, entry "KV
+ * Cache": earlier tokens' keys and values, including a shared prefix, are kept
+ * in fixed-size pages and new tokens attend to them).  The same tensor-core
+ * kernel as attn_fwd, with each 128-key tile gathered from eight pages.
+ *   q            [total_q, Hq, d] bf16: sequence s's chunk is rows
+ *                cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1
+ *   k_cache,
+ *   v_cache      [num_pages, page_size, Hkv, d] bf16, page_table int32
+ *                [num_seqs, max_pages_per_seq] (as attn_decode_paged)
+ *   seq_lens     int32 [num_seqs], DEVICE: cached tokens of sequence s, the chunk's
+ *                own tokens included -- the caller appends the chunk's keys and
+ *                values before the call; chunk query i sits at position
+ *                seq_lens[s] - q_len + i.  Needs q_len <= seq_lens[s] <=
+ *                max_pages_per_seq * page_size; a sequence that breaks this is
+ *                skipped and ATTN_ERR_DEVICE_BOUNDS recorded.
+ *   cu_seqlens_q int32 [num_seqs + 1], DEVICE (as attn_fwd_varlen); max_qlen a
+ *                host-side bound on every q_len.
+ *   o            [total_q, Hq, d] bf16;  lse [Hq, total_q] fp32 or NULL.
+ *   causal != 0: query i sees positions <= its own; else all cached tokens.
+ *   A page id out of range is recorded as ATTN_ERR_DEVICE_BOUNDS and its tokens
+ *   are read as zero keys and values (never from outside the cache).
+ *   Supported: page_size == 16, d in {64, 128}.
+ */
+attn_status_t attn_fwd_chunked_paged(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *page_table, const int32_t *seq_lens,
+                                     const int32_t *cu_seqlens_q, void *o, float *lse,
+                                     int num_seqs, int total_q, int max_qlen, int Hq, int Hkv,
+                                     int d, int page_size, int num_pages, int max_pages_per_seq,
+                                     int causal, float scale, attn_stream_t stream);
+
+/*
  * attn_fwd_f32 -- the same operation with fp32 q, k, v and o (same layouts and
  * rules as attn_fwd).  Arithmetic is fp32 throughout (no reduced-precision
  * tensor-core path).  1 <= d <= 128 and d % 4 == 0.
