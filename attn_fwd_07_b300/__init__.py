@@ -17,6 +17,7 @@ import torch
 
 __all__ = [
     "AttnError", "load_library", "attn_fwd", "attn_fwd_window", "attn_fwd_chunked_paged",
+    "attn_fwd_two_pass",
     "attn_fwd_f32",
     "attn_fwd_varlen", "attn_decode_paged", "attn_decode_paged_window", "attn_decode_paged_fp8",
     "attn_decode_paged_noalloc", "attn_decode_workspace_size", "attn_status_string",
@@ -59,6 +60,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, SZ, P]
+        lib.attn_fwd_two_pass.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_fwd_chunked_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I,
                                                I, I, F, P]
         lib.attn_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
@@ -78,7 +80,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_last_cuda_error.restype = ctypes.c_char_p
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
                      "attn_fwd_window", "attn_decode_paged_window", "attn_decode_paged_fp8",
-                     "attn_fwd_chunked_paged",
+                     "attn_fwd_chunked_paged", "attn_fwd_two_pass",
                      "attn_decode_paged_noalloc", "attn_get_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -208,6 +210,29 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = True,
                                         int(max_seqlen), Hq, Hkv, d, int(bool(causal)),
                                         float(scale), _stream(stream))
     _check(rc, "attn_fwd_varlen")
+    return o, lse
+
+
+def attn_fwd_two_pass(q, k, v, causal: bool = True, scale: float | None = None, o=None,
+                      lse=None, stream=None):
+    """attn_fwd in the two-pass order (row statistics first, then the output); lse is
+    always produced (it carries the statistics between the passes)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [B, N, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_fwd_two_pass(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq,
+                                          Hkv, N, d, int(bool(causal)), float(scale),
+                                          _stream(stream))
+    _check(rc, "attn_fwd_two_pass")
     return o, lse
 
 

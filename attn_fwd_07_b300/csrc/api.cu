@@ -59,6 +59,24 @@ attn_status_t launch_status() {
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
+// Shared-memory size attribute of every instantiation of the tensor-core prefill.
+template <int D>
+cudaError_t prefill_attrs() {
+    const int smem = (int)PrefillCfg<D>::SMEM;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(prefill_tc_kernel<D, false, 0>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(prefill_tc_kernel<D, true, 0>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(prefill_tc_kernel<D, false, 1>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return e;
+    return cudaFuncSetAttribute(prefill_tc_kernel<D, false, 2>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
 // Per-device one-time set-up: SM count, status word address, kernel attributes.
 attn_status_t device_state(DeviceState **out) {
     int dev = 0;
@@ -77,18 +95,7 @@ attn_status_t device_state(DeviceState **out) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)prefill_simt_smem_bytes(kSimtMaxD))) != cudaSuccess)
             return cuda_fail(e);
-        if ((e = cudaFuncSetAttribute(prefill_tc_kernel<128, false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)PrefillCfg<128>::SMEM)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(prefill_tc_kernel<128, true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)PrefillCfg<128>::SMEM)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(prefill_tc_kernel<64, false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)PrefillCfg<64>::SMEM)) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(prefill_tc_kernel<64, true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)PrefillCfg<64>::SMEM)) != cudaSuccess)
+        if ((e = prefill_attrs<128>()) != cudaSuccess || (e = prefill_attrs<64>()) != cudaSuccess)
             return cuda_fail(e);
         if ((e = cudaFuncSetAttribute(decode_split_kernel<true>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -126,6 +133,21 @@ attn_status_t make_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+template <int D>
+void launch_prefill_variant(unsigned grid, const PrefillParams &p, const CUtensorMap &mq,
+                            const CUtensorMap &mk, const CUtensorMap &mv, bool paged, int pass,
+                            cudaStream_t stream) {
+    using C = PrefillCfg<D>;
+    if (paged)
+        prefill_tc_kernel<D, true, 0><<<grid, C::THREADS, C::SMEM, stream>>>(p, mq, mk, mv);
+    else if (pass == 1)
+        prefill_tc_kernel<D, false, 1><<<grid, C::THREADS, C::SMEM, stream>>>(p, mq, mk, mv);
+    else if (pass == 2)
+        prefill_tc_kernel<D, false, 2><<<grid, C::THREADS, C::SMEM, stream>>>(p, mq, mk, mv);
+    else
+        prefill_tc_kernel<D, false, 0><<<grid, C::THREADS, C::SMEM, stream>>>(p, mq, mk, mv);
+}
+
 // Keys and values held in a cache of 16-token pages (chunked prefill).
 struct PagedKV {
     const int32_t *page_table;  // [nseq, maxp]
@@ -141,7 +163,7 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
                                 const int32_t *cu_seqlens, int nseq, int N_or_total,
                                 int ntiles, int Hq, int Hkv, int d, int wl, int wr,
                                 float scale, cudaStream_t stream,
-                                const PagedKV *paged = nullptr) {
+                                const PagedKV *paged = nullptr, int pass = 0) {
     DeviceState *st = nullptr;
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
@@ -196,21 +218,10 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     if (grid == 0) return ATTN_OK;
     const unsigned gx = (unsigned)grid;
-    if (d == 128) {
-        if (paged)
-            prefill_tc_kernel<128, true><<<gx, PrefillCfg<128>::THREADS, PrefillCfg<128>::SMEM,
-                                           stream>>>(p, mq, mk, mv);
-        else
-            prefill_tc_kernel<128, false><<<gx, PrefillCfg<128>::THREADS, PrefillCfg<128>::SMEM,
-                                            stream>>>(p, mq, mk, mv);
-    } else {
-        if (paged)
-            prefill_tc_kernel<64, true><<<gx, PrefillCfg<64>::THREADS, PrefillCfg<64>::SMEM,
-                                          stream>>>(p, mq, mk, mv);
-        else
-            prefill_tc_kernel<64, false><<<gx, PrefillCfg<64>::THREADS, PrefillCfg<64>::SMEM,
-                                           stream>>>(p, mq, mk, mv);
-    }
+    if (d == 128)
+        launch_prefill_variant<128>(gx, p, mq, mk, mv, paged != nullptr, pass, stream);
+    else
+        launch_prefill_variant<64>(gx, p, mq, mk, mv, paged != nullptr, pass, stream);
     return launch_status();
 }
 
@@ -296,6 +307,24 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
     const int ntiles = (max_seqlen + 127) / 128;
     return launch_prefill_tc(q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, ntiles, Hq, Hkv,
                              d, -1, causal ? 0 : -1, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_two_pass(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                                attn_stream_t stream) {
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)B * N * Hq * d > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
+    const int ntiles = (N + 127) / 128;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    attn_status_t s = launch_prefill_tc(q, k, v, o, lse, nullptr, B, N, ntiles, Hq, Hkv, d, -1,
+                                        causal ? 0 : -1, scale, cs, nullptr, 1);
+    if (s != ATTN_OK) return s;
+    return launch_prefill_tc(q, k, v, o, lse, nullptr, B, N, ntiles, Hq, Hkv, d, -1,
+                             causal ? 0 : -1, scale, cs, nullptr, 2);
 }
 
 attn_status_t attn_fwd_chunked_paged(const void *q, const void *k_cache, const void *v_cache,

@@ -113,7 +113,12 @@ enum : uint32_t {
 // table (eight page boxes per 128-key tile, assembled into the same shared-memory
 // layout), queries are a packed chunk per sequence positioned at the end of the
 // sequence's cached tokens.
-template <int D, bool PAGED>
+// PASS: 0 = the one-pass forward above.  The two-pass form of the FlashAttention-1
+// section ("FlashAttention-1 (İki Geçişli Yaklaşım)"): 1 = statistics only (S
+// tiles, running maximum and sum; no V, no PV product) written as LSE = M + ln L;
+// 2 = output with the statistics known (P = 2^(s * scale * log2e - LSE * log2e)
+// needs no running maximum and no rescaling; O = P V).
+template <int D, bool PAGED, int PASS = 0>
 __global__ void __launch_bounds__(384, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
@@ -243,26 +248,37 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             }
             int issued_k = 0, issued_v = 0;
             const int npg = (kvlen + 15) / 16;  // pages holding this sequence's keys
+            // PAGED: page ids of key tile J0 + j (eight 16-token pages), read one tile
+            // ahead so the loads overlap the waits; -1 past the sequence
+            int ids_next[8];
+            auto read_ids = [&](int j) {
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    const int pg = (J0 + j) * 8 + q8;
+                    ids_next[q8] = (j < n_kv && pg < npg)
+                                       ? p.page_table[(long long)sq * p.maxp + pg] : -1;
+                }
+            };
+            if constexpr (PAGED) read_ids(0);
             for (int j = 0; j < n_kv; ++j) {
                 const int kvrow = tok0 + (J0 + j) * C::BN;
-                // PAGED: the tile's eight 16-token pages; a page past the sequence, or a
-                // page id out of range (reported), is loaded from an out-of-range page
-                // coordinate, which the copy fills with zeros
+                // a page past the sequence, or a page id out of range (reported), is
+                // loaded from an out-of-range page coordinate: the copy fills zeros
                 int pcoord[8];
                 if constexpr (PAGED) {
 #pragma unroll
                     for (int q8 = 0; q8 < 8; ++q8) {
                         const int pg = (J0 + j) * 8 + q8;
-                        int pid = p.num_pages;
-                        if (pg < npg) {
-                            pid = p.page_table[(long long)sq * p.maxp + pg];
-                            if ((unsigned)pid >= (unsigned)p.num_pages) {
-                                record_status(p.status, kStatusBounds);
-                                pid = p.num_pages;
-                            }
+                        int pid = ids_next[q8];
+                        if (pg >= npg) {
+                            pid = p.num_pages;
+                        } else if ((unsigned)pid >= (unsigned)p.num_pages) {
+                            record_status(p.status, kStatusBounds);
+                            pid = p.num_pages;
                         }
                         pcoord[q8] = pid;
                     }
+                    read_ids(j + 1);
                 }
                 const int sk = j % C::SK;
                 if (!mbar_wait(bar(BAR_KEMPTY + sk), ((uint32_t)(j / C::SK) & 1u) ^ 1u, p.status,
@@ -283,6 +299,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     }
                 }
                 issued_k = j + 1;
+                if constexpr (PASS == 1) continue;  // the statistics need no values
                 const int sv = j % C::SV;
                 if (!mbar_wait(bar(BAR_VEMPTY + sv), ((uint32_t)(j / C::SV) & 1u) ^ 1u, p.status,
                                abort_flag))
@@ -352,10 +369,13 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     // ring index j counts from J0; tile t's own count from its first key tile
                     const int it = J0 + j - (t ? jlo[1] : jlo[0]);
                     if (uses(t, j)) {
+                        // (statistics pass: PFULL says the S tile has been read)
                         if (!mbar_wait(bar(BAR_PFULL + t), (uint32_t)it & 1u, p.status, abort_flag)) {
                             ok = false;
                             break;
                         }
+                    }
+                    if (PASS != 1 && uses(t, j)) {
                         if (!v_ready) {
                             if (!mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u, p.status,
                                            abort_flag)) {
@@ -390,7 +410,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     }
                 }
                 if (!ok) break;
-                tc_commit(bar(BAR_VEMPTY + sv));
+                if (PASS != 1) tc_commit(bar(BAR_VEMPTY + sv));
                 if (k_ready) tc_commit(bar(BAR_KEMPTY + sk1));
             }
             // all issued MMAs complete before TMEM is released
@@ -414,6 +434,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         float l = 0.f;                             // sum of P (fp32) -> LSE
         float lr = 0.f;                            // sum of bf16-rounded P -> normalises O
         const float sl2 = p.scale_log2;
+        const long long lse_idx = p.cu_seqlens ? (long long)(t ? head[1] : head[0]) * p.total +
+                                                     tok0 + qpos
+                                               : ((long long)batch * p.Hq +
+                                                  (t ? head[1] : head[0])) * p.N + qpos;
+        if constexpr (PASS == 2) {
+            // the row's statistics from the first pass: P = 2^(s * sl2 - LSE * log2e)
+            const float lse_row = qpos < qlen ? p.lse[lse_idx] : 0.f;
+            m_ref = lse_row * kLog2e;
+        }
         bool ok = true;
         for (int j = 0; j < n_mine; ++j) {
             ok = mbar_wait(bar(BAR_SFULL + t), (uint32_t)j & 1u, p.status, abort_flag);
@@ -428,6 +457,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
             tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
             tc_wait_ld();
+            if constexpr (PASS == 1) {
+                // the S tile is in registers: the next one may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
+            }
 
             float *s = reinterpret_cast<float *>(sr);
             const int kv0 = (j_first + j) * C::BN;
@@ -436,7 +471,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 for (int c = 0; c < 128; ++c)
                     if (kv0 + c < klo || kv0 + c > khi) s[c] = -INFINITY;
             }
-            // row maximum: eight independent 3-input max chains
+            // row maximum: eight independent 3-input max chains (the output pass of the
+            // two-pass form knows the row's statistics and skips this)
+            if constexpr (PASS != 2) {
             float mxa[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mxa[i] = fmax3(s[i], s[i + 8], s[i + 16]);
@@ -462,7 +499,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     m_ref = m_new;
                 }
 #pragma unroll 1
-                for (int c = 0; c < D; c += 16) {
+                for (int c = 0; c < (PASS == 1 ? 0 : D); c += 16) {
                     uint32_t orr[16];
                     tmem_ld16(ocol + c, orr);
                     tc_wait_ld();
@@ -472,6 +509,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     tmem_st16(ocol + c, orr);
                 }
             }
+            }  // PASS != 2
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
             // P = 2^(s*scale*log2e - M); the exact row sum feeds the log-sum-exp, and the
             // row sum of the bf16-rounded P (the values the PV product uses) normalises O,
@@ -489,25 +527,36 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_use, -m_use);
                     const float p0 = ex2(t0);
                     const float p1 = ex2(t1);
-                    const uint32_t pp = pack_bf16(p0, p1);
                     const int a = (c >> 1) & 1;
                     fadd2(le[2 * a], le[2 * a + 1], p0, p1);
-                    add_bf16x2_to(lq[a], pp);
-                    pk[(c - cb) >> 1] = pp;
+                    if constexpr (PASS != 1) {
+                        const uint32_t pp = pack_bf16(p0, p1);
+                        add_bf16x2_to(lq[a], pp);
+                        pk[(c - cb) >> 1] = pp;
+                    }
                 }
-                tmem_st16(scol + (cb >> 1), pk);
+                if constexpr (PASS != 1) tmem_st16(scol + (cb >> 1), pk);
             }
             l += (le[0] + le[1]) + (le[2] + le[3]);
             lr += lq[0] + lq[1];
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
+            if constexpr (PASS != 1) {
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
+            }
         }
         if (ok && n_mine > 0) {
-            // ---- epilogue: O / L -> bf16, LSE
-            ok = mbar_wait(bar(BAR_OFULL + t), 0u, p.status, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
+            // ---- epilogue: O / L -> bf16, LSE (statistics pass: LSE only; output pass:
+            // O only, the LSE is its input)
+            if constexpr (PASS == 1) {
+                if (qpos < qlen && p.lse)
+                    p.lse[lse_idx] = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+                ok = false;
+            } else {
+                ok = mbar_wait(bar(BAR_OFULL + t), 0u, p.status, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+            }
             if (ok) {
                 tc_fence_after();
                 const bool row_ok = qpos < qlen;
@@ -534,12 +583,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                                                 pkd[4 * e + 3]);
                     }
                 }
-                if (row_ok && p.lse) {
-                    const float lse = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-                    const long long idx = p.cu_seqlens ? (long long)h * p.total + tok
-                                                       : ((long long)batch * p.Hq + h) * p.N + qpos;
-                    p.lse[idx] = lse;
-                }
+                if (PASS == 0 && row_ok && p.lse)
+                    p.lse[lse_idx] = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
             }
         }
     }

@@ -287,6 +287,12 @@ WORKLOADS = {
         dict(S=8, lo=512, hi=8192, Hq=32, Hkv=8, d=128, dtype=torch.bfloat16, factor=1.0,
              causal=True),
         "8 packed sequences, lengths U[512,8192], Hq=32 Hkv=8 d=128, bf16 N(0,1), causal"),
+    # the long-context GQA workload computed in the two-pass order (statistics, then
+    # output): same inputs as gqa_causal_n16384
+    "gqa_causal_n16384_two_pass": Workload(
+        "gqa_causal_n16384_two_pass", "two_pass", 3,
+        dict(B=1, N=16384, Hq=32, Hkv=8, d=128, dtype=torch.bfloat16, factor=0.5, causal=True),
+        "B=1 Hq=32 Hkv=8 N=16384 d=128, bf16 N(0,1)*0.5, causal, two-pass order"),
     # local attention as the sliding-window glossary entry describes it: w/2 keys on
     # either side of each token, here w = 4096 on an 8192-token sequence (the length
     # the entry uses to count full attention's ~67 million pairs)
@@ -327,7 +333,7 @@ def make(name: str, batch: int | None = None):
     paged workloads) with the same recipe otherwise; None keeps it."""
     w = WORKLOADS[name]
     p = w.params
-    if w.kind == "dense":
+    if w.kind in ("dense", "two_pass"):
         B = p["B"] if batch is None else int(batch)
         return dense(B, p["N"], p["Hq"], p["Hkv"], p["d"], w.seed, p["dtype"], p["factor"],
                      p["causal"])

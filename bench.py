@@ -332,6 +332,9 @@ class Leg:
         elif self.kind == "varlen":
             A.attn_fwd_varlen(d[0], d[1], d[2], d[3], self.max_len, self.w.causal, self.scale,
                               o=self.o, lse=self.lse, stream=stream)
+        elif self.kind == "two_pass":
+            A.attn_fwd_two_pass(d[0], d[1], d[2], self.w.causal, self.scale, o=self.o,
+                                lse=self.lse, stream=stream)
         elif self.f32:
             A.attn_fwd_f32(d[0], d[1], d[2], self.w.causal, self.scale, o=self.o, lse=self.lse,
                            stream=stream)
@@ -360,7 +363,7 @@ class Leg:
 
 
 def launches_per_call(leg) -> int:
-    return 2 if leg.kind in ("decode", "decode_fp8") else 1
+    return 2 if leg.kind in ("decode", "decode_fp8", "two_pass") else 1
 
 
 def cpu_oracle_sample(w, kind: str, seconds: float, seed: int = 0):

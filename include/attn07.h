@@ -99,6 +99,22 @@ attn_status_t attn_fwd_window(const void *q, const void *k, const void *v, void 
                               int window_right, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_two_pass -- attn_fwd computed in the two-pass order that
+ * "Donanıma Duyarlı Algoritma Tasarımı: FlashAttention" (fatihsoysal.com)
+ * describes in section "FlashAttention-1 (İki Geçişli Yaklaşım)": a first pass
+ * over all key tiles computes only each row's maximum M and sum L (no values,
+ * no output), a second pass recomputes Q K^T, normalises with M and L and
+ * accumulates O, with no running rescaling.  Same result as attn_fwd up to
+ * rounding; it repeats the Q K^T work (about 1.5x the tensor work of attn_fwd)
+ * and is kept as an independent evaluation order.  The statistics travel
+ * between the passes in `lse` (LSE = M + ln L), which is therefore required:
+ * lse == NULL returns ATTN_ERR_INVALID_ARG.  Arguments otherwise as attn_fwd.
+ */
+attn_status_t attn_fwd_two_pass(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                                attn_stream_t stream);
+
+/*
  * attn_fwd_chunked_paged -- a chunk of new queries per sequence against that
  * sequence's paged key/value cache: chunked prefill, and prefill after a reused
  * (cached) prompt prefix (yapayzekasozluk.tr "attention" tag page, entry "KV
