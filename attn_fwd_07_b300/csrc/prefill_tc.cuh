@@ -452,27 +452,71 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             }
             tc_fence_after();
             uint32_t sr[128];
-            tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-            tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-            tc_wait_ld();
+            float *s = reinterpret_cast<float *>(sr);
+            const int kv0 = (j_first + j) * C::BN;
+            // the S row from TMEM, keys outside [klo, khi] masked
+            auto load_s = [&]() {
+                tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+                tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+                tc_wait_ld();
+                if (kv0 < klo || kv0 + C::BN - 1 > khi) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (kv0 + c < klo || kv0 + c > khi) s[c] = -INFINITY;
+                }
+            };
+            load_s();
             if constexpr (PASS == 1) {
                 // the S tile is in registers: the next one may overwrite it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
             }
-
-            float *s = reinterpret_cast<float *>(sr);
-            const int kv0 = (j_first + j) * C::BN;
-            if (kv0 < klo || kv0 + C::BN - 1 > khi) {
+            bool p_done = false;
+            if constexpr (PASS == 0) {
+                // Fast path: try P against the current reference maximum first.  If no
+                // row's sum of P over this tile exceeds 2^24, no element exceeds the
+                // reference by more than 24 (log2 units): P, the sums and O stay far
+                // inside the fp32/bf16 range (relative precision does not depend on the
+                // scale), so the reference stands and the row maximum is never needed.
+                // Otherwise reload the S tile (it is still in TMEM) and take the path
+                // with the maximum below, which moves the reference when it is exceeded
+                // by more than 8.
+                if (__all_sync(0xffffffffu, j > 0 && m_ref != -INFINITY)) {
+                    float fe[4] = {0.f, 0.f, 0.f, 0.f};
+                    float fq[2] = {0.f, 0.f};
+                    uint32_t pk[64];
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (kv0 + c < klo || kv0 + c > khi) s[c] = -INFINITY;
+                    for (int c = 0; c < 128; c += 2) {
+                        float t0, t1;
+                        ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_ref, -m_ref);
+                        const float p0 = ex2(t0);
+                        const float p1 = ex2(t1);
+                        const int a = (c >> 1) & 1;
+                        fadd2(fe[2 * a], fe[2 * a + 1], p0, p1);
+                        const uint32_t pp = pack_bf16(p0, p1);
+                        add_bf16x2_to(fq[a], pp);
+                        pk[c >> 1] = pp;
+                    }
+                    const float lt = (fe[0] + fe[1]) + (fe[2] + fe[3]);
+                    if (__all_sync(0xffffffffu, lt <= 16777216.f)) {
+                        l += lt;
+                        lr += fq[0] + fq[1];
+                        tmem_st16(scol + 0, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+                        tmem_st16(scol + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+                        tmem_st16(scol + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
+                        tmem_st16(scol + 48, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
+                        p_done = true;
+                    } else {
+                        load_s();
+                    }
+                }
             }
             // row maximum: eight independent 3-input max chains (the output pass of the
             // two-pass form knows the row's statistics and skips this)
+            if (!p_done) {
             if constexpr (PASS != 2) {
             float mxa[8];
 #pragma unroll
@@ -539,6 +583,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             }
             l += (le[0] + le[1]) + (le[2] + le[3]);
             lr += lq[0] + lq[1];
+            }  // !p_done
             if constexpr (PASS != 1) {
                 tc_wait_st();
                 tc_fence_before();
