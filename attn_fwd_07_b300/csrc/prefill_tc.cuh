@@ -343,11 +343,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 const uint32_t qb = base + C::OFF_Q + t * C::TILE;
                 const uint32_t kb = base + C::OFF_K + (j % C::SK) * C::TILE;
                 const uint32_t dcol = tmem + (t ? C::COL_S1 : C::COL_S0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk >> 2) * C::HALF + (uint32_t)(kk & 3) * 32u;
-                    tc_mma_ss(dcol, smem_desc_sw128(qb + off, 1024, 1024),
-                              smem_desc_sw128(kb + off, 1024, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                // descriptors built once per product; each of the D/16 steps advances the
+                // start address by a constant (32 bytes within a 64-dim half, 16 KB between)
+                const SmemDesc qd = smem_desc_parts(qb, 1024, 1024);
+                const SmemDesc kd = smem_desc_parts(kb, 1024, 1024);
+                tc_mma_ss_off<0, 0>(dcol, qd, kd, idesc_qk, 0u);
+                tc_mma_ss_off<32, 32>(dcol, qd, kd, idesc_qk, 1u);
+                tc_mma_ss_off<64, 64>(dcol, qd, kd, idesc_qk, 1u);
+                tc_mma_ss_off<96, 96>(dcol, qd, kd, idesc_qk, 1u);
+                if constexpr (D == 128) {
+                    tc_mma_ss_off<C::HALF, C::HALF>(dcol, qd, kd, idesc_qk, 1u);
+                    tc_mma_ss_off<C::HALF + 32, C::HALF + 32>(dcol, qd, kd, idesc_qk, 1u);
+                    tc_mma_ss_off<C::HALF + 64, C::HALF + 64>(dcol, qd, kd, idesc_qk, 1u);
+                    tc_mma_ss_off<C::HALF + 96, C::HALF + 96>(dcol, qd, kd, idesc_qk, 1u);
                 }
                 tc_commit(bar(BAR_SFULL + t));
             };
@@ -389,11 +397,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                         const uint32_t vb = base + C::OFF_V + sv * C::TILE;
                         const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
                         const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
-    #pragma unroll
-                        for (int kk = 0; kk < C::BN / 16; ++kk)
-                            tc_mma_ts(ocol, pcol + kk * 8,
-                                      smem_desc_sw128(vb + kk * 2048u, C::HALF, 1024), idesc_pv,
-                                      (it > 0 || kk > 0) ? 1u : 0u);
+                        const SmemDesc vd = smem_desc_parts(vb, C::HALF, 1024);
+                        tc_mma_ts_off<0>(ocol, pcol, vd, idesc_pv, it > 0 ? 1u : 0u);
+                        tc_mma_ts_off<2048>(ocol, pcol + 8, vd, idesc_pv, 1u);
+                        tc_mma_ts_off<4096>(ocol, pcol + 16, vd, idesc_pv, 1u);
+                        tc_mma_ts_off<6144>(ocol, pcol + 24, vd, idesc_pv, 1u);
+                        tc_mma_ts_off<8192>(ocol, pcol + 32, vd, idesc_pv, 1u);
+                        tc_mma_ts_off<10240>(ocol, pcol + 40, vd, idesc_pv, 1u);
+                        tc_mma_ts_off<12288>(ocol, pcol + 48, vd, idesc_pv, 1u);
+                        tc_mma_ts_off<14336>(ocol, pcol + 56, vd, idesc_pv, 1u);
                         if (!uses(t, j + 1)) tc_commit(bar(BAR_OFULL + t));
                     }
                     if (uses(t, j + 1)) {

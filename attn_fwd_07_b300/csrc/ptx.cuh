@@ -289,6 +289,47 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
            | ((M >> 4) << 24);  // M / 16
 }
 
+// A shared-memory matrix descriptor held as its two 32-bit halves; the start
+// address (16-byte units) is bits 0..13 of lo.
+struct SmemDesc {
+    uint32_t lo, hi;
+};
+
+__device__ __forceinline__ SmemDesc smem_desc_parts(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = smem_desc_sw128(addr, lbo, sbo);
+    return SmemDesc{(uint32_t)d, (uint32_t)(d >> 32)};
+}
+
+// tc_mma_ss with the descriptors' start addresses advanced by the compile-time
+// offsets AOFF / BOFF (bytes, multiples of 16): one 32-bit add per operand (the
+// address field cannot carry out for shared-memory addresses below 256 KB).
+template <uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void tc_mma_ss_off(uint32_t d_tmem, SmemDesc a, SmemDesc b,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 alo, blo;\n\t.reg .b64 da, db;\n\t"
+        "add.u32 alo, %1, %7;\n\tadd.u32 blo, %3, %8;\n\t"
+        "mov.b64 da, {alo, %2};\n\tmov.b64 db, {blo, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate), "n"(AOFF >> 4),
+        "n"(BOFF >> 4)
+        : "memory");
+}
+
+// tc_mma_ts with the B descriptor's start address advanced by BOFF bytes.
+template <uint32_t BOFF>
+__device__ __forceinline__ void tc_mma_ts_off(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 blo;\n\t.reg .b64 db;\n\t"
+        "add.u32 blo, %2, %6;\n\tmov.b64 db, {blo, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate), "n"(BOFF >> 4)
+        : "memory");
+}
+
 // ------------------------------------------------------------------ shared memory
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
