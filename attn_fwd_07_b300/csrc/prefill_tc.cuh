@@ -371,7 +371,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int sv = j % C::SV;
                 const int sk1 = (j + 1) % C::SK;
-                bool v_ready = false, k_ready = false;
+                // the value tile of this step and the key tile of the next are waited for
+                // first: they are normally in place, and checking them while the softmax
+                // still works keeps those checks off the path from P to the next product
+                // (every key tile of [J0, J1] is used by at least one query tile)
+                const bool k_ready = j + 1 < n_kv;
+                if (PASS != 1 && !mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u,
+                                            p.status, abort_flag))
+                    break;
+                if (k_ready && !mbar_wait(bar(BAR_KFULL + sk1), (uint32_t)((j + 1) / C::SK) & 1u,
+                                          p.status, abort_flag))
+                    break;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     // ring index j counts from J0; tile t's own count from its first key tile
@@ -384,14 +394,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                         }
                     }
                     if (PASS != 1 && uses(t, j)) {
-                        if (!v_ready) {
-                            if (!mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u, p.status,
-                                           abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            v_ready = true;
-                        }
                         tc_fence_after();
                         // O_t += P_t V_j: P_t (bf16, 128 x 128) from the S_t columns of TMEM
                         const uint32_t vb = base + C::OFF_V + sv * C::TILE;
@@ -409,15 +411,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                         if (!uses(t, j + 1)) tc_commit(bar(BAR_OFULL + t));
                     }
                     if (uses(t, j + 1)) {
-                        if (!k_ready) {
-                            if (!mbar_wait(bar(BAR_KFULL + sk1), (uint32_t)((j + 1) / C::SK) & 1u,
-                                           p.status, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            k_ready = true;
-                            tc_fence_after();
-                        }
+                        tc_fence_after();
                         issue_qk(t, j + 1);
                     }
                 }

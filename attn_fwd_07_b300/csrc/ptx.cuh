@@ -85,6 +85,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait polling with the non-blocking test (no suspension): the waiter sees the
+// phase complete within a few cycles, at the price of issue slots while it spins.
+// For a single latency-critical thread.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, unsigned *status,
+                                               volatile int *abort) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (abort && *abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                record_status(status, kStatusTimeout);
+                if (abort) *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // (after recording a timeout) if it did not complete within kWaitLimitNs, or
 // if *abort (shared flag, may be null) became non-zero meanwhile.
