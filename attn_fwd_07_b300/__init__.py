@@ -56,6 +56,8 @@ def load_library(path: str = LIB_PATH):
         lib = ctypes.CDLL(path)
         P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.attn_release_host_staging.argtypes = []
         lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
@@ -81,7 +83,8 @@ def load_library(path: str = LIB_PATH):
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
                      "attn_fwd_window", "attn_decode_paged_window", "attn_decode_paged_fp8",
                      "attn_fwd_chunked_paged", "attn_fwd_two_pass",
-                     "attn_decode_paged_noalloc", "attn_get_device_status"):
+                     "attn_decode_paged_noalloc", "attn_get_device_status", "attn_fwd_host",
+                     "attn_release_host_staging"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -139,6 +142,39 @@ def attn_fwd(q, k, v, causal: bool = True, scale: float | None = None, o=None, l
                                  d, int(bool(causal)), float(scale), _stream(stream))
     _check(rc, "attn_fwd")
     return o, lse
+
+
+def attn_fwd_host(q, k, v, causal: bool = True, scale: float | None = None, o=None, lse=None,
+                  want_lse: bool = True, stream=None):
+    """attn_fwd on HOST tensors: q [B,N,Hq,d], k/v [B,N,Hkv,d] bf16 CPU tensors (page-locked
+    for overlapped copies) -> (o, lse) CPU tensors, complete on return.  The library copies
+    them through a device staging area, overlapping the copies with the compute."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not (t.device.type == "cpu" and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise ValueError("%s must be a contiguous CPU bfloat16 tensor" % n)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k/v must be [B, N, Hkv, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = q.is_pinned()
+    if o is None:
+        o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=pin)
+    for t, n, dt in ((o, "o", torch.bfloat16), (lse, "lse", torch.float32)):
+        if t is not None and not (t.device.type == "cpu" and t.dtype == dt and t.is_contiguous()):
+            raise ValueError("%s must be a contiguous CPU %s tensor" % (n, dt))
+    rc = load_library().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                      N, d, int(bool(causal)), float(scale), _stream(stream))
+    _check(rc, "attn_fwd_host")
+    return o, lse
+
+
+def attn_release_host_staging():
+    """Free the device staging area that attn_fwd_host keeps between calls."""
+    _check(load_library().attn_release_host_staging(), "attn_release_host_staging")
 
 
 def attn_fwd_window(q, k, v, window_left: int, window_right: int, scale: float | None = None,

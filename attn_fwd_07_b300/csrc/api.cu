@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
@@ -163,7 +164,7 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
                                 const int32_t *cu_seqlens, int nseq, int N_or_total,
                                 int ntiles, int Hq, int Hkv, int d, int wl, int wr,
                                 float scale, cudaStream_t stream,
-                                const PagedKV *paged = nullptr, int pass = 0) {
+                                const PagedKV *paged = nullptr, int pass = 0, int tile0 = 0) {
     DeviceState *st = nullptr;
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
@@ -203,6 +204,7 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.ntiles = ntiles;
+    p.tile0 = tile0;
     // a CTA takes two query heads of one group on the same rows when the group size is
     // even, else two consecutive row tiles of one head
     p.head_pairs = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
@@ -561,6 +563,229 @@ attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_cache, cons
     return attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
                              page_size, num_pages, max_pages_per_seq, scale, scratch,
                              (size_t)ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// ---------------------------------------------------------------- prefill from host memory
+// attn_fwd_host: the work is cut into G groups of consecutive key/value heads (with their
+// query heads).  Group c's Q/K/V slices are copied into one of NB device buffer sets on
+// the copy-in stream, attention runs on the caller's stream, and the O/LSE slices go back
+// on the copy-out stream; events order the three, so the copy in of group c + 1, the
+// compute of group c and the copy out of group c - 1 overlap (a host-to-device copy,
+// a kernel and a device-to-host copy use different engines).
+namespace {
+
+constexpr int kHostMaxGroups = 16;
+constexpr int kHostSets = 2;
+
+struct HostStaging {
+    void *buf = nullptr;
+    size_t bytes = 0;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t e_in[kHostMaxGroups], e_comp[kHostMaxGroups], e_out[kHostMaxGroups];
+    bool ready = false;
+};
+std::mutex g_host_mu;
+HostStaging g_host[kMaxDevices];
+
+attn_status_t host_staging_init(HostStaging &h) {
+    if (h.ready) return ATTN_OK;
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e);
+    for (int c = 0; c < kHostMaxGroups; ++c) {
+        if ((e = cudaEventCreateWithFlags(&h.e_in[c], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h.e_comp[c], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h.e_out[c], cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    h.ready = true;
+    return ATTN_OK;
+}
+
+void host_staging_release(HostStaging &h) {
+    if (!h.ready) return;
+    cudaStreamSynchronize(h.s_in);
+    cudaStreamSynchronize(h.s_out);
+    if (h.buf) cudaFree(h.buf);
+    h.buf = nullptr;
+    h.bytes = 0;
+    for (int c = 0; c < kHostMaxGroups; ++c) {
+        cudaEventDestroy(h.e_in[c]);
+        cudaEventDestroy(h.e_comp[c]);
+        cudaEventDestroy(h.e_out[c]);
+    }
+    cudaStreamDestroy(h.s_in);
+    cudaStreamDestroy(h.s_out);
+    h.ready = false;
+}
+
+inline size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Number of key/value head groups: a divisor of Hkv, at most 4 (each group then moves
+// at least a quarter of the tensors per copy call), at least 1.
+int host_groups(int Hkv) {
+    for (int g = 4; g > 1; --g)
+        if (Hkv % g == 0) return g;
+    return 1;
+}
+
+}  // namespace
+
+attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                            attn_stream_t stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)B * N * Hq * d > (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostStaging &h = g_host[dev];
+    attn_status_t st = host_staging_init(h);
+    if (st != ATTN_OK) return st;
+    cudaStream_t sc = reinterpret_cast<cudaStream_t>(stream);
+    auto reserve = [&](size_t bytes) -> attn_status_t {
+        if (h.bytes >= bytes) return ATTN_OK;
+        cudaError_t e2;
+        if (h.buf) {
+            if ((e2 = cudaFree(h.buf)) != cudaSuccess) return cuda_fail(e2);
+            h.buf = nullptr;
+            h.bytes = 0;
+        }
+        if ((e2 = cudaMalloc(&h.buf, bytes)) != cudaSuccess) return cuda_fail(e2);
+        h.bytes = bytes;
+        return ATTN_OK;
+    };
+    const char *hq_src = static_cast<const char *>(q);
+    const char *hk_src = static_cast<const char *>(k);
+    const char *hv_src = static_cast<const char *>(v);
+    char *ho = static_cast<char *>(o);
+    const size_t rows = (size_t)B * N;
+    // the copies wait for work the caller queued on its stream before this call
+    if ((e = cudaEventRecord(h.e_out[0], sc)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(h.s_in, h.e_out[0], 0)) != cudaSuccess) return cuda_fail(e);
+
+    if (causal) {
+        // Causal: query rows [n0, n1) need keys [0, n1) only, so the work is cut along
+        // the sequence.  Chunk c's rows of Q, K and V (contiguous per sequence) are
+        // copied in order; its query tiles run once chunks 0..c are in place; its rows
+        // of O and LSE go back while later chunks are copied in and computed.
+        const size_t tq = (size_t)Hq * d * 2, tkv = (size_t)Hkv * d * 2;  // bytes per token
+        const size_t q_bytes = round256(rows * tq), kv_bytes = round256(rows * tkv);
+        const size_t lse_bytes = lse ? round256(rows * Hq * 4) : 0;
+        if ((st = reserve(2 * q_bytes + 2 * kv_bytes + lse_bytes)) != ATTN_OK) return st;
+        char *dq = static_cast<char *>(h.buf), *dout = dq + q_bytes, *dk = dout + q_bytes;
+        char *dv = dk + kv_bytes;
+        float *dlse = lse ? reinterpret_cast<float *>(dv + kv_bytes) : nullptr;
+        const int ntiles = (N + 127) / 128;
+        // pieces of whole 256-row pairs of tiles, about sixteen of them: the last piece's
+        // compute and copy out are all that is left once the copies in are done
+        const int tiles_per = std::max(2, ((ntiles + 15) / 16 + 1) & ~1);
+        const int C = (ntiles + tiles_per - 1) / tiles_per;
+        for (int c = 0; c < C && st == ATTN_OK; ++c) {
+            const int t0 = c * tiles_per, t1 = std::min(ntiles, t0 + tiles_per);
+            const size_t n0 = (size_t)t0 * 128, n1 = std::min((size_t)N, (size_t)t1 * 128);
+            const size_t nr = n1 - n0;
+            if ((e = cudaMemcpy2DAsync(dq + n0 * tq, (size_t)N * tq, hq_src + n0 * tq, (size_t)N * tq,
+                                       nr * tq, B, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
+                (e = cudaMemcpy2DAsync(dk + n0 * tkv, (size_t)N * tkv, hk_src + n0 * tkv,
+                                       (size_t)N * tkv, nr * tkv, B, cudaMemcpyHostToDevice,
+                                       h.s_in)) != cudaSuccess ||
+                (e = cudaMemcpy2DAsync(dv + n0 * tkv, (size_t)N * tkv, hv_src + n0 * tkv,
+                                       (size_t)N * tkv, nr * tkv, B, cudaMemcpyHostToDevice,
+                                       h.s_in)) != cudaSuccess ||
+                (e = cudaEventRecord(h.e_in[c], h.s_in)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(sc, h.e_in[c], 0)) != cudaSuccess) {
+                st = cuda_fail(e);
+                break;
+            }
+            st = launch_prefill_tc(dq, dk, dv, dout, dlse, nullptr, B, N, t1 - t0, Hq, Hkv, d, -1,
+                                   0, scale, sc, nullptr, 0, t0);
+            if (st != ATTN_OK) break;
+            if ((e = cudaEventRecord(h.e_comp[c], sc)) != cudaSuccess ||
+                (e = cudaStreamWaitEvent(h.s_out, h.e_comp[c], 0)) != cudaSuccess ||
+                (e = cudaMemcpy2DAsync(ho + n0 * tq, (size_t)N * tq, dout + n0 * tq, (size_t)N * tq,
+                                       nr * tq, B, cudaMemcpyDeviceToHost, h.s_out)) != cudaSuccess ||
+                (lse && (e = cudaMemcpy2DAsync(lse + n0, (size_t)N * 4, dlse + n0, (size_t)N * 4,
+                                               nr * 4, (size_t)B * Hq, cudaMemcpyDeviceToHost,
+                                               h.s_out)) != cudaSuccess))
+                st = cuda_fail(e);
+        }
+    } else {
+        // Full attention: every row needs every key, so the work is cut by groups of
+        // key/value heads (with their query heads) over two device buffer sets.
+        const int G = host_groups(Hkv);
+        const int hk = Hkv / G, hq = Hq / G;
+        const size_t row_q = (size_t)hq * d * 2, row_kv = (size_t)hk * d * 2;  // per token
+        const size_t q_bytes = round256(rows * row_q), kv_bytes = round256(rows * row_kv);
+        const size_t lse_bytes = lse ? round256((size_t)B * hq * N * 4) : 0;
+        const size_t set_bytes = 2 * q_bytes + 2 * kv_bytes + lse_bytes;  // Q, O, K, V, LSE
+        if ((st = reserve(kHostSets * set_bytes)) != ATTN_OK) return st;
+        for (int c = 0; c < G && st == ATTN_OK; ++c) {
+            char *set = static_cast<char *>(h.buf) + (size_t)(c % kHostSets) * set_bytes;
+            char *dq = set, *dout = set + q_bytes, *dk = set + 2 * q_bytes;
+            char *dv = dk + kv_bytes;
+            float *dlse = lse ? reinterpret_cast<float *>(dv + kv_bytes) : nullptr;
+            // copy in: the set's inputs are free once the compute of group c - NB is done
+            if (c >= kHostSets &&
+                (e = cudaStreamWaitEvent(h.s_in, h.e_comp[c - kHostSets], 0)) != cudaSuccess)
+                st = cuda_fail(e);
+            if (st == ATTN_OK &&
+                ((e = cudaMemcpy2DAsync(dq, row_q, hq_src + (size_t)c * row_q, (size_t)Hq * d * 2,
+                                        row_q, rows, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
+                 (e = cudaMemcpy2DAsync(dk, row_kv, hk_src + (size_t)c * row_kv, (size_t)Hkv * d * 2,
+                                        row_kv, rows, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
+                 (e = cudaMemcpy2DAsync(dv, row_kv, hv_src + (size_t)c * row_kv, (size_t)Hkv * d * 2,
+                                        row_kv, rows, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
+                 (e = cudaEventRecord(h.e_in[c], h.s_in)) != cudaSuccess))
+                st = cuda_fail(e);
+            // compute: after its inputs, and once the copy out of group c - NB freed O / LSE
+            if (st == ATTN_OK && (e = cudaStreamWaitEvent(sc, h.e_in[c], 0)) != cudaSuccess)
+                st = cuda_fail(e);
+            if (st == ATTN_OK && c >= kHostSets &&
+                (e = cudaStreamWaitEvent(sc, h.e_out[c - kHostSets], 0)) != cudaSuccess)
+                st = cuda_fail(e);
+            if (st == ATTN_OK)
+                st = attn_fwd(dq, dk, dv, dout, dlse, B, hq, hk, N, d, 0, scale, stream);
+            if (st == ATTN_OK && (e = cudaEventRecord(h.e_comp[c], sc)) != cudaSuccess)
+                st = cuda_fail(e);
+            // copy out: O rows into the group's head slice, LSE [B, Hq, N] rows of this group
+            if (st == ATTN_OK &&
+                ((e = cudaStreamWaitEvent(h.s_out, h.e_comp[c], 0)) != cudaSuccess ||
+                 (e = cudaMemcpy2DAsync(ho + (size_t)c * row_q, (size_t)Hq * d * 2, dout, row_q,
+                                        row_q, rows, cudaMemcpyDeviceToHost, h.s_out)) != cudaSuccess ||
+                 (lse && (e = cudaMemcpy2DAsync(lse + (size_t)c * hq * N, (size_t)Hq * N * 4, dlse,
+                                                (size_t)hq * N * 4, (size_t)hq * N * 4, (size_t)B,
+                                                cudaMemcpyDeviceToHost, h.s_out)) != cudaSuccess) ||
+                 (e = cudaEventRecord(h.e_out[c], h.s_out)) != cudaSuccess))
+                st = cuda_fail(e);
+        }
+    }
+    // o and lse are complete (or the call failed) when both copy streams and the compute
+    // stream have drained; nothing of this call is left in flight
+    cudaError_t e1 = cudaStreamSynchronize(h.s_in);
+    cudaError_t e2 = cudaStreamSynchronize(sc);
+    cudaError_t e3 = cudaStreamSynchronize(h.s_out);
+    if (st == ATTN_OK && e1 != cudaSuccess) st = cuda_fail(e1);
+    if (st == ATTN_OK && e2 != cudaSuccess) st = cuda_fail(e2);
+    if (st == ATTN_OK && e3 != cudaSuccess) st = cuda_fail(e3);
+    return st;
+}
+
+attn_status_t attn_release_host_staging(void) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    host_staging_release(g_host[dev]);
+    return ATTN_OK;
 }
 
 }  // extern "C"

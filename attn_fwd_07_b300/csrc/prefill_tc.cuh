@@ -63,7 +63,8 @@ struct PrefillParams {
     int nseq;       // dense: B; varlen: num_seqs
     int total;      // varlen: total tokens
     int Hq, Hkv;
-    int ntiles;     // 128-row query tiles per sequence (of the longest sequence)
+    int ntiles;     // 128-row query tiles per sequence (of the longest sequence) to run
+    int tile0;      // the first of them: tiles [tile0, tile0 + ntiles) of each sequence
     int head_pairs; // 1: a CTA takes two heads of a group on the same rows; 0: two row tiles
     int wl, wr;     // query i sees keys i - wl .. i + wr; -1: no limit on that side
                     // (causal: wl = -1, wr = 0; full: wl = wr = -1)
@@ -160,17 +161,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     if (p.head_pairs) {
         head[0] = 2 * hu;
         head[1] = 2 * hu + 1;
-        row0[0] = row0[1] = outer * C::BM;
+        row0[0] = row0[1] = (p.tile0 + outer) * C::BM;
     } else {
         head[0] = head[1] = hu;
-        row0[0] = 2 * outer * C::BM;
+        row0[0] = (p.tile0 + 2 * outer) * C::BM;
         row0[1] = row0[0] + C::BM;
     }
+    const int row_end = min(qlen, (p.tile0 + p.ntiles) * C::BM);  // rows this launch runs
     const int g = head[0] / (p.Hq / p.Hkv);
     bool valid[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        valid[t] = outer >= 0 && row0[t] < qlen;
+        valid[t] = outer >= 0 && row0[t] < row_end;
         const int last_row = min(row0[t] + C::BM, qlen) - 1;
         const int lo_key = p.wl < 0 ? 0 : max(0, qoff + row0[t] - p.wl);
         const int hi_key = p.wr < 0 ? kvlen - 1 : min(kvlen - 1, qoff + last_row + p.wr);

@@ -25,8 +25,10 @@
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers, owned by the caller; the
- *     library allocates, frees and synchronises nothing (the single exception
- *     is attn_get_device_status, which synchronises `stream` by design).
+ *     library allocates, frees and synchronises nothing.  Two exceptions by
+ *     design: attn_get_device_status synchronises `stream`, and attn_fwd_host
+ *     (HOST pointers) keeps a device staging area and returns when its outputs
+ *     are written.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) and runs asynchronously; the return value reports argument
  *     validation and launch errors only.
@@ -81,6 +83,39 @@ typedef enum {
 attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                        int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                        attn_stream_t stream);
+
+/*
+ * attn_fwd_host -- attn_fwd with every tensor in HOST memory: q, k, v are read
+ * from the host, o and lse are written to the host, and the call returns when
+ * they hold the result (or an error).  Same layouts, sizes, values and errors
+ * as attn_fwd, except that the pointers need no alignment and are host
+ * pointers (page-locked memory lets the copies run asynchronously; pageable
+ * memory works, with the copies serialised by the driver).
+ * How: inputs are copied to the device on a library stream, attention runs on
+ * `stream`, results are copied back on a second library stream, in pieces
+ * ordered by events so that copy in, compute and copy out overlap.  Causal:
+ * the pieces are runs of about a sixteenth of the sequence (whole 256-row
+ * query tile pairs); rows [n0, n1) need keys [0, n1) only, so a piece's query tiles
+ * run as soon as its own rows and the earlier ones are on the device.  Full
+ * attention: the pieces are up to four groups of key/value heads (a divisor of
+ * Hkv) with their query heads, over two device buffer sets.  Either way every
+ * row's result is bitwise the one attn_fwd gives on the whole tensors (a row's
+ * arithmetic depends on neither the other rows' tiles nor the other heads).
+ * Device memory: a staging area per device (the whole tensors for a causal
+ * call; two groups' slices for full attention), allocated on first use, grown
+ * when a larger call needs it, and kept for the next call;
+ * attn_release_host_staging frees it.
+ * Calls on one device are serialised by a lock.  Work the caller queued on
+ * `stream` before the call completes before the copies start.
+ */
+attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                            attn_stream_t stream);
+
+/* Frees the current device's attn_fwd_host staging area and its streams and
+ * events (after the copies in flight, if any, have finished).  Returns ATTN_OK,
+ * or ATTN_ERR_CUDA if the current device cannot be read. */
+attn_status_t attn_release_host_staging(void);
 
 /*
  * attn_fwd_window -- attn_fwd with local ("sliding window") attention: query i

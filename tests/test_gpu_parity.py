@@ -104,6 +104,33 @@ def test_prefill_adversarial(oracle, kind):
         assert_close(errors(f32(o), o_ref, f32(lse), lse_ref), (kind, causal))
 
 
+@pytest.mark.parametrize("keys", [(40,), (100,), (150,), (230,), (300,), (480,), (150, 480),
+                                  (230, 480), (229, 230)])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (1, 1)])
+def test_prefill_maximum_jumps_inside_a_key_tile(oracle, keys, Hq, Hkv):
+    """Every query shares a direction u; the listed keys are 32 u, so their scores sit
+    about 33 (log2 units) above the rest.  A key in the first or second 64-key half of
+    a key tile that is not the row's first moves the row maximum in the middle of the
+    tile (the exponent reference is exceeded by far more than the half-tile bound), a
+    key in the first tile sets it; two keys move it twice.  Both CTA pairings (two
+    heads of a group, two row tiles)."""
+    B, N, d = 1, 512, 128
+    w = inputs.dense(B, N, Hq, Hkv, d, 95, torch.float32)
+    u = torch.full((d,), 0.25)
+    q = w.q * 0.3 + u
+    k = w.k.clone()
+    for key in keys:
+        k[:, key] = u * 32.0
+    # V halved so that |O| (about one V row here) stays below 2.2
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, w.v * 0.5))
+    for causal in (False, True):
+        o, lse = A.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal, w.scale)
+        torch.cuda.synchronize()
+        check_status()
+        o_ref, lse_ref = oracle.attn_fwd(f32(q), f32(k), f32(v), causal, w.scale)
+        assert_close(errors(f32(o), o_ref, f32(lse), lse_ref), (keys, Hq, causal))
+
+
 # ---------------------------------------------------------------- fp32 (CUDA cores)
 
 @pytest.mark.parametrize("B,N,Hq,Hkv,d,causal", [
