@@ -358,9 +358,17 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run, mx);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                const float alpha = ex2(m_run - m_use);
+                // the exponent's reference maximum moves only when the row maximum exceeds
+                // it by more than 8 (log2 units): until then P <= 2^8, exact in range for
+                // fp32, f16 and bf16, and O and the sums need no rescaling this page
+                const bool need = mx > m_run + 8.f;
+                const bool any_need = __any_sync(0xffffffffu, need);
+                float alpha = 1.f;
+                if (any_need && need) {
+                    alpha = ex2(m_run - mx);
+                    m_run = mx;
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
                 float pr[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) pr[j] = ex2(sv[j] - m_use);
@@ -377,8 +385,9 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 ps += __shfl_xor_sync(0xffffffffu, ps, 2);
                 l_run = l_run * alpha + ps;   // exact sum -> log-sum-exp
                 q_run = q_run * alpha + pq;   // sum of the rounded P -> normalises O
-                m_run = m_new;
-                if constexpr (FP8) {
+                if (!any_need) {
+                    // no row of the warp moved its reference: O stands
+                } else if constexpr (FP8) {
                     // O^T tiles: columns are query heads 2 quad and 2 quad + 1, whose
                     // factors live in lanes 8 quad and 8 quad + 4
                     const float ae = __shfl_sync(0xffffffffu, alpha, 8 * quad);
