@@ -390,7 +390,8 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_p
         return 0;
     DeviceState *st = nullptr;
     if (device_state(&st) != ATTN_OK) return 0;
-    const size_t slots = (size_t)B + (size_t)st->sms;
+    // one slot per sequence plus one per CTA of the split kernel (up to two per SM)
+    const size_t slots = (size_t)B + (size_t)kDecMaxCtasPerSm * st->sms;
     const size_t bytes_o = slots * Hq * d * sizeof(float);
     const size_t bytes_l = slots * Hq * sizeof(float);
     return ((bytes_o + 255) & ~(size_t)255) + bytes_l;
@@ -430,7 +431,11 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
     const size_t stage = dec_stage_bytes(Hkv, d, fp8);
-    int stages = (int)((220 * 1024 - 2048) / stage);
+    // FP8 pages are half the bytes and twice the conversion work per byte: two CTAs per
+    // SM (sixteen consumer warps) with half the ring each hide more of the consumers'
+    // latency; the bf16 kernel keeps one CTA per SM and the deeper ring
+    const int ctas_per_sm = fp8 ? 2 : 1;
+    int stages = (int)(((fp8 ? 108 : 220) * 1024 - 2048) / stage);
     if (stages > kDecMaxStages) stages = kDecMaxStages;
     if (stages < 2) return ATTN_ERR_UNSUPPORTED;
     // cache as a 4-D tensor: (dim, token-in-page, head, page) so that one box
@@ -448,7 +453,7 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     if ((s = make_map(&mk, k_cache, 4, dims, strides, box, dt)) != ATTN_OK) return s;
     if ((s = make_map(&mv, v_cache, 4, dims, strides, box, dt)) != ATTN_OK) return s;
 
-    const size_t slots = (size_t)B + (size_t)st->sms;
+    const size_t slots = (size_t)B + (size_t)kDecMaxCtasPerSm * st->sms;
     DecodeParams p;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.page_table = page_table;
@@ -471,7 +476,7 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     p.window = window < 0 ? -1 : window;
     p.scale_log2 = scale * kLog2e;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const int G = st->sms;
+    const int G = st->sms * ctas_per_sm;
     const size_t smem = dec_smem_bytes(Hkv, d, stages, fp8);
     if (fp8)
         decode_split_kernel<true><<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);

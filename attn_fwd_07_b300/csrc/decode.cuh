@@ -42,6 +42,7 @@ namespace attn07 {
 constexpr int kDecPage = 16;          // tokens per page (the kernel is built for it)
 constexpr int kDecMaxStages = 8;
 constexpr int kDecMaxHkv = 8;
+constexpr int kDecMaxCtasPerSm = 2;    // the FP8 kernel runs two CTAs per SM
 
 struct DecodeParams {
     const __nv_bfloat16 *q;    // [B, Hq, d]
@@ -117,7 +118,7 @@ __host__ __device__ __forceinline__ bool dec_range_nonempty(long long c, long lo
 // them to f16 (exact) and runs the products with f16 operands; per-head scales
 // multiply the scores and the output.
 template <bool FP8>
-__global__ void __launch_bounds__(32 * (kDecMaxHkv + 1), 1)
+__global__ void __launch_bounds__(32 * (kDecMaxHkv + 1), FP8 ? 2 : 1)
 decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ uint8_t dec_smem_raw[];
