@@ -229,8 +229,8 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
  *   workspace   device scratch of at least attn_decode_workspace_size(...) bytes,
  *               16-byte aligned, owned by the caller; its contents on entry do
  *               not matter and are overwritten.
- *   Supported: page_size == 16, d in {64, 128}, Hq/Hkv <= 8, Hkv <= 16 (and one
- *   page of keys plus values for all heads must fit three times in shared memory).
+ *   Supported: page_size == 16, d in {64, 128}, Hq/Hkv <= 8, Hkv <= 8 (one
+ *   consumer warp per key/value head); other sizes return ATTN_ERR_UNSUPPORTED.
  *   A page id outside [0, num_pages) is not read: its tokens are treated as
  *   masked and ATTN_ERR_DEVICE_BOUNDS is recorded for attn_get_device_status.
  *   A sequence with seq_lens[b] == 0 gets O = 0, LSE = -inf.
