@@ -85,7 +85,27 @@ def test_varlen_and_decode_validation(lib):
     bad_g = list(args)
     bad_g[8], bad_g[9] = 64, 4
     assert lib.attn_decode_paged(*bad_g, p, 1 << 30, None) == A.ATTN_ERR_UNSUPPORTED
+    many_kv = list(args)       # 16 key/value heads: one consumer warp each would exceed 8
+    many_kv[8], many_kv[9] = 32, 16
+    assert lib.attn_decode_paged(*many_kv, p, 1 << 30, None) == A.ATTN_ERR_UNSUPPORTED
     assert lib.attn_decode_workspace_size(0, 32, 8, 128, 10, 16) == 0
+
+
+def test_host_entry_validation(lib):
+    # attn_fwd_host rejects bad arguments before any CUDA call (host pointers need no
+    # alignment, so an odd address passes that check and fails nothing else)
+    P = ctypes.c_void_p
+    h = P((1 << 20) + 3)
+    assert lib.attn_fwd_host(None, h, h, h, None, 1, 4, 2, 8, 128, 1, 0.1,
+                             None) == A.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_host(h, h, h, h, None, 1, 4, 3, 8, 128, 1, 0.1,
+                             None) == A.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_host(h, h, h, h, None, 1, 4, 2, 0, 128, 1, 0.1,
+                             None) == A.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_host(h, h, h, h, None, 1, 4, 2, 8, 128, 1, float("inf"),
+                             None) == A.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_host(h, h, h, h, None, 1, 4, 2, 8, 96, 1, 0.1,
+                             None) == A.ATTN_ERR_UNSUPPORTED
 
 
 def test_binding_requires_library(tmp_path):
