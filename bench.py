@@ -518,10 +518,17 @@ def run_reference(args):
 L2_BYTES = 126 * 1024 * 1024
 
 
+# fp32 CUDA-core peak (no measured figure exists for it): 148 SMs x 128 fp32 lanes x 2 FLOP
+# per fused multiply-add x 2032 MHz, the maximum SM clock
+ALU_F32_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
 def roofline(leg, launch_ms, peaks, peak_src):
     if leg.bound == "alu":
-        return None  # fp32 CUDA-core path: launch-latency bound at its workload
-    if leg.bound == "tensor":
+        r = {"bound": "alu", "achieved": leg.rate(leg.work, launch_ms), "peak": ALU_F32_TFLOPS,
+             "unit": "TFLOP/s",
+             "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2032 MHz"}
+    elif leg.bound == "tensor":
         r = {"bound": "tensor", "achieved": leg.rate(leg.work, launch_ms),
              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
              "peak_source": "%s bf16 burst (cuBLAS)" % peak_src}

@@ -58,3 +58,28 @@ def test_reference_arm_nonzero_rank_does_nothing(monkeypatch, capsys):
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_roofline_bounds_and_fractions():
+    """bench.roofline: achieved = work / time in the leg's unit, frac = achieved / peak, for
+    the three bounds (the fp32 path's ALU peak is derived: 148 x 128 x 2 x 2.032 GHz)."""
+    import bench
+
+    class Leg:
+        work, unit, kernel, name = 2e12, "TFLOP/s", "prefill_simt_kernel", "nothing"
+
+        def rate(self, work, ms):
+            return work / (ms * 1e-3) / 1e12
+
+    peaks = {"bf16_tflops": 1800.0, "hbm_gbs": 6400.0}
+    leg = Leg()
+    for bound, peak in (("alu", 148 * 128 * 2 * 2.032e9 / 1e12), ("tensor", 1800.0)):
+        leg.bound = bound
+        r = bench.roofline(leg, 2.0, peaks, "measured")
+        assert r["bound"] == bound and r["unit"] == "TFLOP/s"
+        assert abs(r["achieved"] - 1000.0) < 1e-9 and abs(r["peak"] - peak) < 1e-9
+        assert abs(r["frac"] - 1000.0 / peak) < 1e-12
+    leg.bound, leg.unit = "hbm", "GB/s"
+    leg.rate = lambda work, ms: work / (ms * 1e-3) / 1e9
+    r = bench.roofline(leg, 2.0, peaks, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and abs(r["frac"] - 1e6 / 6400.0) < 1e-9
