@@ -33,22 +33,6 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-    uint32_t l;
-    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-    return l;
-}
-
-__device__ __forceinline__ bool elect_one() {
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "elect.sync _|p, 0xffffffff;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(pred));
-    return pred != 0;
-}
-
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -57,10 +41,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -85,38 +65,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// mbar_wait polling with the non-blocking test (no suspension): the waiter sees the
-// phase complete within a few cycles, at the price of issue slots while it spins.
-// For a single latency-critical thread.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, unsigned *status,
-                                               volatile int *abort) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (abort && *abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                record_status(status, kStatusTimeout);
-                if (abort) *abort = 1;
-                return false;
-            }
-        }
-    }
-}
-
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // (after recording a timeout) if it did not complete within kWaitLimitNs, or
 // if *abort (shared flag, may be null) became non-zero meanwhile.
@@ -137,25 +85,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
-// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a multiple
-// of 32).  Every thread that takes part must reach it: it has no time bound.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
-                                            int c0, int c1, int c2, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
@@ -177,12 +110,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_normal() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -287,14 +214,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-        : "memory");
-}
-
 // Shared-memory matrix descriptor for tcgen05 (K-major or MN-major operand,
 // 128-byte swizzle).  addr: byte address in shared memory (the tile's atoms
 // must sit on 1024-byte boundaries); lbo/sbo: leading/stride byte offsets.
@@ -373,13 +292,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
-                                       uint32_t w) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
-                 "r"(w)
-                 : "memory");
-}
-
 // ------------------------------------------------------------------ mma.sync
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
@@ -456,15 +368,6 @@ __device__ __forceinline__ float f16hi(uint32_t v) {
     asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}"
         : "=f"(f) : "r"(v));
     return f;
-}
-
-// Two FP8 E4M3 values (bits 0..7 and 8..15 of x) to f16x2 (exact: every E4M3
-// value is an f16 value); the value in bits 0..7 lands in bits 0..15.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
-    uint32_t r;
-    asm("{\n\t.reg .b16 v;\n\tcvt.u16.u32 v, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, v;\n\t}"
-        : "=r"(r) : "r"(x));
-    return r;
 }
 
 // Four FP8 E4M3 values (bytes 0..3 of x) to two f16x2: bytes 0, 1 -> lo, bytes 2, 3 -> hi.
