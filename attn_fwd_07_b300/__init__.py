@@ -58,6 +58,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_release_host_staging.argtypes = []
+        lib.attn_selftest_wait_timeout.argtypes = [P, P]
         lib.attn_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
@@ -84,7 +85,7 @@ def load_library(path: str = LIB_PATH):
                      "attn_fwd_window", "attn_decode_paged_window", "attn_decode_paged_fp8",
                      "attn_fwd_chunked_paged", "attn_fwd_two_pass",
                      "attn_decode_paged_noalloc", "attn_get_device_status", "attn_fwd_host",
-                     "attn_release_host_staging"):
+                     "attn_release_host_staging", "attn_selftest_wait_timeout"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -170,6 +171,17 @@ def attn_fwd_host(q, k, v, causal: bool = True, scale: float | None = None, o=No
                                       N, d, int(bool(causal)), float(scale), _stream(stream))
     _check(rc, "attn_fwd_host")
     return o, lse
+
+
+def attn_selftest_wait_timeout(stream=None):
+    """Run the device check of the pipeline-wait bound (about 2 s); returns the two
+    waits' elapsed nanoseconds.  Afterwards attn_get_device_status() reports the
+    timeout once."""
+    out = (ctypes.c_ulonglong * 2)()
+    _check(load_library().attn_selftest_wait_timeout(ctypes.cast(out, ctypes.c_void_p),
+                                                     _stream(stream)),
+           "attn_selftest_wait_timeout")
+    return int(out[0]), int(out[1])
 
 
 def attn_release_host_staging():

@@ -17,6 +17,7 @@
 #include "decode.cuh"
 #include "prefill_simt.cuh"
 #include "prefill_tc.cuh"
+#include "selftest.cuh"
 
 using namespace attn07;
 
@@ -568,6 +569,43 @@ attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_cache, cons
     return attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
                              page_size, num_pages, max_pages_per_seq, scale, scratch,
                              (size_t)ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// ---------------------------------------------------------------- wait-bound self-test
+// Result words of selftest_wait_timeout_kernel (a fixed device array: the check needs
+// no allocation and runs on whatever device is current).
+static __device__ unsigned long long g_selftest_out[4];
+
+attn_status_t attn_selftest_wait_timeout(unsigned long long *elapsed_ns, attn_stream_t stream) {
+    DeviceState *st = nullptr;
+    attn_status_t s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    void *dout = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&dout, g_selftest_out);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    selftest_wait_timeout_kernel<<<1, 64, 0, cs>>>(st->status,
+                                                   static_cast<unsigned long long *>(dout));
+    if ((s = launch_status()) != ATTN_OK) return s;
+    unsigned long long h[4];
+    if ((e = cudaMemcpyFromSymbolAsync(h, g_selftest_out, sizeof(h), 0, cudaMemcpyDeviceToHost,
+                                       cs)) != cudaSuccess)
+        return cuda_fail(e);
+    if ((e = cudaStreamSynchronize(cs)) != cudaSuccess) return cuda_fail(e);
+    if (elapsed_ns) {
+        elapsed_ns[0] = h[1];
+        elapsed_ns[1] = h[3];
+    }
+    // as designed: neither wait succeeded; warp 0 ran to the bound, warp 1 left on the
+    // abort flag before its own bound (kSelftestStaggerNs + kWaitLimitNs after the start)
+    const bool as_designed = h[0] == 0 && h[2] == 0 && h[1] >= kWaitLimitNs &&
+                             h[3] < kSelftestStaggerNs + kWaitLimitNs;
+    if (!as_designed) {
+        snprintf(g_last_cuda_error, sizeof(g_last_cuda_error),
+                 "wait self-test: results %llu %llu, %llu ns and %llu ns", h[0], h[2], h[1], h[3]);
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
 }
 
 // ---------------------------------------------------------------- prefill from host memory

@@ -306,6 +306,25 @@ const char *attn_status_string(attn_status_t s);
 attn_status_t attn_get_device_status(attn_stream_t stream);
 
 /*
+ * attn_selftest_wait_timeout -- checks on the device that a pipeline wait whose
+ * arrival never comes ends in an error the host can read, not in a hang or a
+ * fault.  Every wait of the attention kernels goes through the same bounded
+ * wait: after 2 s it records a timeout in the device status word, raises its
+ * CTA's abort flag so that the CTA's other waits end too, and lets the kernel
+ * return.  This runs one CTA of two waiting warps on barriers nothing arrives
+ * on.  Warp 0 waits first and runs to the bound.  Warp 1 starts its wait 0.5 s
+ * later and must leave on the abort flag before its own bound.  The call takes
+ * about 2 s and synchronises `stream`.
+ *   elapsed_ns  host array of 2, or NULL: nanoseconds from the kernel's start
+ *               to the end of warp 0's and warp 1's waits.
+ * Returns ATTN_OK when both waits ended as described (the status word then
+ * holds the timeout: attn_get_device_status returns ATTN_ERR_TIMEOUT once, and
+ * the device stays usable), ATTN_ERR_CUDA otherwise (attn_last_cuda_error says
+ * what was seen).
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned long long *elapsed_ns, attn_stream_t stream);
+
+/*
  * attn_decode_paged_noalloc -- attn_decode_paged for callers that cannot
  * allocate device memory: a host that hands the library only its input and
  * output buffers (a plugin interface with no workspace to lend), or a serving
