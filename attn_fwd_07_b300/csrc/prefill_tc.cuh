@@ -37,6 +37,9 @@
 // TMEM, mask (causal diagonal / sequence end), running maximum, P = 2^(S *
 // scale * log2e - M) rounded to bf16 and written back over the S columns it
 // came from (P is the A operand of the PV product, read from TMEM), row sums.
+// After a row's first key tile the maximum is first skipped: P is taken against
+// the standing reference M, and only if some row's P sums past 2^24 on this tile
+// is the S row reloaded and the step redone with its maximum.
 //
 // Rescaling: the row maximum used in the exponent only moves when the new
 // maximum exceeds it by more than 8 (log2 units).  Until then P may reach

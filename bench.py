@@ -34,6 +34,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -169,9 +170,19 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: bytes) -> bytes:
+    """C/C++/CUDA source without comments, blank lines or trailing spaces: what a
+    comment-only edit leaves unchanged (string literals in these sources hold no
+    comment markers)."""
+    t = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    t = re.sub(rb"//[^\n]*", b"", t)
+    lines = [ln.rstrip() for ln in t.split(b"\n")]
+    return b"\n".join(ln for ln in lines if ln)
+
+
 def kernel_fingerprint(kernel: str, read=None) -> str:
-    """sha256 (16 hex digits) over the kernel's source files.  `read(name) -> bytes`
-    defaults to the working tree's attn_fwd_07_b300/csrc/<name>."""
+    """sha256 (16 hex digits) over the code of the kernel's source files, comments left
+    out.  `read(name) -> bytes` defaults to the working tree's attn_fwd_07_b300/csrc/<name>."""
     if read is None:
         def read(name):
             with open(os.path.join(ROOT, "attn_fwd_07_b300", "csrc", name), "rb") as f:
@@ -179,7 +190,7 @@ def kernel_fingerprint(kernel: str, read=None) -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
         h.update(name.encode())
-        h.update(read(name))
+        h.update(_code_only(read(name)))
     return h.hexdigest()[:16]
 
 

@@ -83,3 +83,19 @@ def test_roofline_bounds_and_fractions():
     leg.rate = lambda work, ms: work / (ms * 1e-3) / 1e9
     r = bench.roofline(leg, 2.0, peaks, "measured")
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and abs(r["frac"] - 1e6 / 6400.0) < 1e-9
+
+
+def test_kernel_fingerprint_ignores_comments_only():
+    """A comment-only edit keeps a kernel's source fingerprint (the committed ncu traffic
+    still applies); a code edit changes it."""
+    import bench
+    base = {"prefill_tc.cuh": b"int f() {\n  return 1;  // one\n}\n", "ptx.cuh": b"/* x */ int g;\n"}
+
+    def reader(files):
+        return lambda name: files[name]
+
+    fp = bench.kernel_fingerprint("prefill_tc_kernel", reader(base))
+    commented = dict(base, **{"prefill_tc.cuh": b"// header\nint f() {\n\n  return 1;\n}\n"})
+    assert bench.kernel_fingerprint("prefill_tc_kernel", reader(commented)) == fp
+    edited = dict(base, **{"prefill_tc.cuh": b"int f() {\n  return 2;\n}\n"})
+    assert bench.kernel_fingerprint("prefill_tc_kernel", reader(edited)) != fp
