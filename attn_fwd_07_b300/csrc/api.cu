@@ -665,6 +665,16 @@ void host_staging_release(HostStaging &h) {
 
 inline size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// `height` rows of `width` bytes, `spitch` / `dpitch` bytes apart: one plain copy when the
+// rows are contiguous on both sides (or there is one row, where a pitch would only have
+// to satisfy the 2-D copy's pitch limit for nothing), else a 2-D copy.
+cudaError_t copy_rows(void *dst, size_t dpitch, const void *src, size_t spitch, size_t width,
+                      size_t height, cudaMemcpyKind kind, cudaStream_t stream) {
+    if (height == 1 || (dpitch == width && spitch == width))
+        return cudaMemcpyAsync(dst, src, width * height, kind, stream);
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, kind, stream);
+}
+
 // Number of key/value head groups: a divisor of Hkv, at most 4 (each group then moves
 // at least a quarter of the tensors per copy call), at least 1.
 int host_groups(int Hkv) {
@@ -735,12 +745,12 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
             const int t0 = c * tiles_per, t1 = std::min(ntiles, t0 + tiles_per);
             const size_t n0 = (size_t)t0 * 128, n1 = std::min((size_t)N, (size_t)t1 * 128);
             const size_t nr = n1 - n0;
-            if ((e = cudaMemcpy2DAsync(dq + n0 * tq, (size_t)N * tq, hq_src + n0 * tq, (size_t)N * tq,
+            if ((e = copy_rows(dq + n0 * tq, (size_t)N * tq, hq_src + n0 * tq, (size_t)N * tq,
                                        nr * tq, B, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
-                (e = cudaMemcpy2DAsync(dk + n0 * tkv, (size_t)N * tkv, hk_src + n0 * tkv,
+                (e = copy_rows(dk + n0 * tkv, (size_t)N * tkv, hk_src + n0 * tkv,
                                        (size_t)N * tkv, nr * tkv, B, cudaMemcpyHostToDevice,
                                        h.s_in)) != cudaSuccess ||
-                (e = cudaMemcpy2DAsync(dv + n0 * tkv, (size_t)N * tkv, hv_src + n0 * tkv,
+                (e = copy_rows(dv + n0 * tkv, (size_t)N * tkv, hv_src + n0 * tkv,
                                        (size_t)N * tkv, nr * tkv, B, cudaMemcpyHostToDevice,
                                        h.s_in)) != cudaSuccess ||
                 (e = cudaEventRecord(h.e_in[c], h.s_in)) != cudaSuccess ||
@@ -753,9 +763,9 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
             if (st != ATTN_OK) break;
             if ((e = cudaEventRecord(h.e_comp[c], sc)) != cudaSuccess ||
                 (e = cudaStreamWaitEvent(h.s_out, h.e_comp[c], 0)) != cudaSuccess ||
-                (e = cudaMemcpy2DAsync(ho + n0 * tq, (size_t)N * tq, dout + n0 * tq, (size_t)N * tq,
+                (e = copy_rows(ho + n0 * tq, (size_t)N * tq, dout + n0 * tq, (size_t)N * tq,
                                        nr * tq, B, cudaMemcpyDeviceToHost, h.s_out)) != cudaSuccess ||
-                (lse && (e = cudaMemcpy2DAsync(lse + n0, (size_t)N * 4, dlse + n0, (size_t)N * 4,
+                (lse && (e = copy_rows(lse + n0, (size_t)N * 4, dlse + n0, (size_t)N * 4,
                                                nr * 4, (size_t)B * Hq, cudaMemcpyDeviceToHost,
                                                h.s_out)) != cudaSuccess))
                 st = cuda_fail(e);
@@ -780,11 +790,11 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
                 (e = cudaStreamWaitEvent(h.s_in, h.e_comp[c - kHostSets], 0)) != cudaSuccess)
                 st = cuda_fail(e);
             if (st == ATTN_OK &&
-                ((e = cudaMemcpy2DAsync(dq, row_q, hq_src + (size_t)c * row_q, (size_t)Hq * d * 2,
+                ((e = copy_rows(dq, row_q, hq_src + (size_t)c * row_q, (size_t)Hq * d * 2,
                                         row_q, rows, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
-                 (e = cudaMemcpy2DAsync(dk, row_kv, hk_src + (size_t)c * row_kv, (size_t)Hkv * d * 2,
+                 (e = copy_rows(dk, row_kv, hk_src + (size_t)c * row_kv, (size_t)Hkv * d * 2,
                                         row_kv, rows, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
-                 (e = cudaMemcpy2DAsync(dv, row_kv, hv_src + (size_t)c * row_kv, (size_t)Hkv * d * 2,
+                 (e = copy_rows(dv, row_kv, hv_src + (size_t)c * row_kv, (size_t)Hkv * d * 2,
                                         row_kv, rows, cudaMemcpyHostToDevice, h.s_in)) != cudaSuccess ||
                  (e = cudaEventRecord(h.e_in[c], h.s_in)) != cudaSuccess))
                 st = cuda_fail(e);
@@ -801,9 +811,9 @@ attn_status_t attn_fwd_host(const void *q, const void *k, const void *v, void *o
             // copy out: O rows into the group's head slice, LSE [B, Hq, N] rows of this group
             if (st == ATTN_OK &&
                 ((e = cudaStreamWaitEvent(h.s_out, h.e_comp[c], 0)) != cudaSuccess ||
-                 (e = cudaMemcpy2DAsync(ho + (size_t)c * row_q, (size_t)Hq * d * 2, dout, row_q,
+                 (e = copy_rows(ho + (size_t)c * row_q, (size_t)Hq * d * 2, dout, row_q,
                                         row_q, rows, cudaMemcpyDeviceToHost, h.s_out)) != cudaSuccess ||
-                 (lse && (e = cudaMemcpy2DAsync(lse + (size_t)c * hq * N, (size_t)Hq * N * 4, dlse,
+                 (lse && (e = copy_rows(lse + (size_t)c * hq * N, (size_t)Hq * N * 4, dlse,
                                                 (size_t)hq * N * 4, (size_t)hq * N * 4, (size_t)B,
                                                 cudaMemcpyDeviceToHost, h.s_out)) != cudaSuccess) ||
                  (e = cudaEventRecord(h.e_out[c], h.s_out)) != cudaSuccess))
