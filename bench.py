@@ -605,6 +605,14 @@ def run_gpu(args):
                                  for s in range(args.steps)), world, dev) for i in range(nl)]
     leg_val = [legs[i].rate(sum_over_ranks(legs[i].work * args.steps, world, dev), leg_ms[i])
                for i in range(nl)]
+    # the distribution of one leg's per-step device time: median and 90th percentile
+    # (each the maximum over ranks)
+    step_ms = []
+    for i in range(nl):
+        t = sorted(evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps))
+        p90 = t[min(len(t) - 1, int(math.ceil(0.9 * len(t))) - 1)]
+        step_ms.append({"median": max_over_ranks(statistics.median(t), world, dev),
+                        "p90": max_over_ranks(p90, world, dev)})
 
     # ---- end to end through the public API: pinned host inputs in, results out, timed
     n_e2e = max(1, min(args.steps, args.e2e_steps))
@@ -661,9 +669,11 @@ def run_gpu(args):
         }
         line["%s_ms_per_step" % ("decode" if p0.kind.startswith("decode") else "prefill")] = \
             leg_ms[0] / args.steps
+        line["step_ms"] = step_ms[0]
         for i in range(1, nl):
             line[legs[i].kind] = {"value": leg_val[i], "unit": legs[i].unit,
                                   "ms_per_step": leg_ms[i] / args.steps,
+                                  "step_ms": step_ms[i],
                                   "roofline": roofs[i], "e2e": e2e[i]}
         print(json.dumps(line), flush=True)
     if world > 1:
