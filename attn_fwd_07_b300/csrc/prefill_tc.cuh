@@ -486,6 +486,26 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
             }
             bool p_done = false;
+            if constexpr (PASS == 1) {
+                // Statistics pass, fast path: while the reference stands only the sum of P
+                // is needed (same bound as below).  The S row stays in registers (no P is
+                // stored), so a tile whose sum passes 2^24 goes on to the maximum below.
+                if (__all_sync(0xffffffffu, j > 0 && m_ref != -INFINITY)) {
+                    float fe[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 128; c += 2) {
+                        float t0, t1;
+                        ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_ref, -m_ref);
+                        const int a = (c >> 1) & 1;
+                        fadd2(fe[2 * a], fe[2 * a + 1], ex2(t0), ex2(t1));
+                    }
+                    const float lt = (fe[0] + fe[1]) + (fe[2] + fe[3]);
+                    if (__all_sync(0xffffffffu, lt <= 16777216.f)) {
+                        l += lt;
+                        p_done = true;
+                    }
+                }
+            }
             if constexpr (PASS == 0) {
                 // Fast path: try P against the current reference maximum first.  If no
                 // row's sum of P over this tile exceeds 2^24, no element exceeds the
