@@ -130,3 +130,19 @@ def test_cuda_failure_text_is_recorded(lib):
     assert text.startswith("cuda") and "no CUDA error recorded" not in text, text
     with pytest.raises(A.AttnError, match=r"CUDA error \(status 3\) \[cuda"):
         A._check(A.ATTN_ERR_CUDA, "attn_fwd")
+
+
+def test_binding_checks_tensors_before_calling_the_library():
+    """The ctypes binding refuses CPU, mistyped, non-contiguous or mis-shaped tensors with a
+    ValueError before any call into the library (so no device is needed to see it)."""
+    import torch
+    q = torch.zeros((1, 8, 4, 128), dtype=torch.bfloat16)
+    k = torch.zeros((1, 8, 2, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        A.attn_fwd(q, k, k)                       # host tensors for the device entry point
+    with pytest.raises(ValueError, match="CPU bfloat16"):
+        A.attn_fwd_host(q.float(), k, k)          # wrong dtype for the host entry point
+    with pytest.raises(ValueError, match="CPU bfloat16"):
+        A.attn_fwd_host(q.transpose(1, 2), k, k)  # not contiguous
+    with pytest.raises(ValueError, match="matching q"):
+        A.attn_fwd_host(q, k[:, :4], k)           # k with another sequence length
