@@ -99,3 +99,33 @@ def test_kernel_fingerprint_ignores_comments_only():
     assert bench.kernel_fingerprint("prefill_tc_kernel", reader(commented)) == fp
     edited = dict(base, **{"prefill_tc.cuh": b"int f() {\n  return 2;\n}\n"})
     assert bench.kernel_fingerprint("prefill_tc_kernel", reader(edited)) != fp
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores) prints one JSON line
+    with the keys and types the benchmark contract names, on the same metric as our arm."""
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--workload", "single_head_f32", "--steps", "3", "--warmup", "3",
+                          "--ref-seconds", "1"], capture_output=True, text=True, timeout=300,
+                         cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    import bench
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    for key, typ in (("value", float), ("unit", str), ("n_gpus", int), ("steps", int),
+                     ("warmup", int), ("ms_per_step", float), ("higher_is_better", bool),
+                     ("scaling", str), ("dtype", str), ("data", str), ("config", dict),
+                     ("cpu_baseline", dict), ("e2e", dict)):
+        assert isinstance(d[key], typ), (key, d.get(key))
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
+    assert d["vs_baseline"] is None
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
