@@ -72,7 +72,7 @@ def load_library(path: str = LIB_PATH):
                                                  P, SZ, P]
         lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
                                                   P]
-        lib.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.attn_decode_workspace_size.argtypes = [I, I, I, I, I]
         lib.attn_decode_workspace_size.restype = SZ
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -312,9 +312,10 @@ def attn_fwd_chunked_paged(q, k_cache, v_cache, page_table, seq_lens, cu_seqlens
     return o, lse
 
 
-def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, d: int, max_pages_per_seq: int,
+def attn_decode_workspace_size(B: int, Hq: int, d: int, max_pages_per_seq: int,
                                page_size: int) -> int:
-    return int(load_library().attn_decode_workspace_size(B, Hq, Hkv, d, max_pages_per_seq,
+    """Bytes of workspace attn_decode_paged (and its window / FP8 forms) needs."""
+    return int(load_library().attn_decode_workspace_size(B, Hq, d, max_pages_per_seq,
                                                          page_size))
 
 
@@ -335,7 +336,7 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | 
         o = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    need = attn_decode_workspace_size(B, Hq, Hkv, d, maxp, ps)
+    need = attn_decode_workspace_size(B, Hq, d, maxp, ps)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     rc = load_library().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table),
@@ -369,7 +370,7 @@ def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq
         o = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    need = attn_decode_workspace_size(B, Hq, Hkv, d, maxp, ps)
+    need = attn_decode_workspace_size(B, Hq, d, maxp, ps)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     rc = load_library().attn_decode_paged_fp8(
@@ -398,7 +399,7 @@ def attn_decode_paged_window(q, k_cache, v_cache, page_table, seq_lens, window: 
         o = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    need = attn_decode_workspace_size(B, Hq, Hkv, d, maxp, ps)
+    need = attn_decode_workspace_size(B, Hq, d, maxp, ps)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     rc = load_library().attn_decode_paged_window(

@@ -14,6 +14,7 @@
 #include <string.h>
 
 #include "attn07.h"
+#include "attn07_testing.h"
 #include "decode.cuh"
 #include "prefill_simt.cuh"
 #include "prefill_tc.cuh"
@@ -358,7 +359,7 @@ attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float
                            attn_stream_t stream) {
     if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
-    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
     if (d > kSimtMaxD || d % 16 != 0) return ATTN_ERR_UNSUPPORTED;
     if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
@@ -385,10 +386,8 @@ attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float
     return launch_status();
 }
 
-size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_per_seq,
-                                  int page_size) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || max_pages_per_seq <= 0 || page_size <= 0)
-        return 0;
+size_t attn_decode_workspace_size(int B, int Hq, int d, int max_pages_per_seq, int page_size) {
+    if (B <= 0 || Hq <= 0 || d <= 0 || max_pages_per_seq <= 0 || page_size <= 0) return 0;
     DeviceState *st = nullptr;
     if (device_state(&st) != ATTN_OK) return 0;
     // one slot per sequence plus one per CTA of the split kernel (up to two per SM)
@@ -410,7 +409,8 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
                                 const int32_t *page_table, const int32_t *seq_lens, void *o,
                                 float *lse, int B, int Hq, int Hkv, int d, int page_size,
                                 int num_pages, int max_pages_per_seq, int window, float scale,
-                                void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+                                void *workspace, size_t workspace_bytes, attn_stream_t stream,
+                                int ctas = 0) {
     const bool fp8 = k_scale != nullptr;
     if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o || !workspace)
         return ATTN_ERR_INVALID_ARG;
@@ -418,19 +418,18 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 ||
         num_pages <= 0 || max_pages_per_seq <= 0)
         return ATTN_ERR_INVALID_ARG;
-    if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
         !aligned16(workspace))
         return ATTN_ERR_INVALID_ARG;
     if (page_size != kDecPage || (d != 64 && d != 128) || Hkv > kDecMaxHkv || Hq / Hkv > 8)
         return ATTN_ERR_UNSUPPORTED;
     if (fp8 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, d, max_pages_per_seq, page_size);
-    if (need == 0) return ATTN_ERR_CUDA;
-    if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
     DeviceState *st = nullptr;
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
+    const size_t need = attn_decode_workspace_size(B, Hq, d, max_pages_per_seq, page_size);
+    if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
     const size_t stage = dec_stage_bytes(Hkv, d, fp8);
     // FP8 pages are half the bytes and twice the conversion work per byte: two CTAs per
     // SM (sixteen consumer warps) with half the ring each hide more of the consumers'
@@ -477,7 +476,9 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     p.window = window < 0 ? -1 : window;
     p.scale_log2 = scale * kLog2e;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const int G = st->sms * ctas_per_sm;
+    // the workspace has a slot per CTA for up to kDecMaxCtasPerSm CTAs per SM
+    if (ctas < 0 || ctas > kDecMaxCtasPerSm * st->sms) return ATTN_ERR_UNSUPPORTED;
+    const int G = ctas > 0 ? ctas : st->sms * ctas_per_sm;
     const size_t smem = dec_smem_bytes(Hkv, d, stages, fp8);
     if (fp8)
         decode_split_kernel<true><<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
@@ -529,6 +530,24 @@ attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const
                              workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------- test hook
+// attn_decode_paged with the split kernel's CTA count chosen by the caller (declared in
+// attn07_testing.h, not part of the interface): the merged result must not depend on how
+// the pages are cut into CTA ranges, which tests check at counts the length mix of a
+// workload would not produce by itself.
+attn_status_t attn_testing_decode_paged_ctas(const void *q, const void *k_cache,
+                                             const void *v_cache, const int32_t *page_table,
+                                             const int32_t *seq_lens, void *o, float *lse, int B,
+                                             int Hq, int Hkv, int d, int page_size, int num_pages,
+                                             int max_pages_per_seq, float scale, void *workspace,
+                                             size_t workspace_bytes, int ctas,
+                                             attn_stream_t stream) {
+    if (ctas <= 0) return ATTN_ERR_INVALID_ARG;
+    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, page_table, seq_lens, o, lse,
+                             B, Hq, Hkv, d, page_size, num_pages, max_pages_per_seq, -1, scale,
+                             workspace, workspace_bytes, stream, ctas);
+}
+
 // ---------------------------------------------------------------- no-allocation decode
 // Scratch for attn_decode_paged_noalloc: a fixed device array that every GPU
 // loading this library holds until exit.  Host code only ever sees a host-side
@@ -547,13 +566,16 @@ attn_status_t attn_decode_paged_noalloc(const void *q, const void *k_cache, cons
                                         float scale, attn_stream_t stream) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0)
         return ATTN_ERR_INVALID_ARG;
-    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, d, max_pages_per_seq, page_size);
-    if (need == 0) return ATTN_ERR_CUDA;
+    // the device's set-up first, so that its own status (an unusable device, a device
+    // index past the library's table) is what the caller sees
+    DeviceState *st = nullptr;
+    attn_status_t s = device_state(&st);
+    if (s != ATTN_OK) return s;
+    const size_t need = attn_decode_workspace_size(B, Hq, d, max_pages_per_seq, page_size);
     if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mu);

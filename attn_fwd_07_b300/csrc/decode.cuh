@@ -86,17 +86,29 @@ inline size_t dec_smem_bytes(int Hkv, int d, int stages, bool fp8) {
            dec_ctrl_bytes();
 }
 
+// Whether seq_lens[b] is a length the page table can hold: 0 <= len <= maxp * 16.
+__device__ __forceinline__ bool dec_len_ok(const DecodeParams &p, int b) {
+    const int len = p.seq_lens[b];
+    return len >= 0 && (long long)len <= (long long)p.maxp * kDecPage;
+}
+
+// Cached tokens of sequence b; a length outside what the page table holds counts
+// as 0 (the sequence is treated as empty and its table row is never read).
+__device__ __forceinline__ int dec_len(const DecodeParams &p, int b) {
+    return dec_len_ok(p, b) ? p.seq_lens[b] : 0;
+}
+
 // First token the query of sequence b attends to: len - 1 - window under a
 // window, else 0.
 __device__ __forceinline__ int dec_first_token(const DecodeParams &p, int b) {
-    const int len = p.seq_lens[b];
+    const int len = dec_len(p, b);
     return (p.window >= 0 && len - 1 - p.window > 0) ? len - 1 - p.window : 0;
 }
 
 // Pages of sequence b that hold attended tokens: logical pages
 // first_token / 16 .. ceil(len / 16) - 1.
 __device__ __forceinline__ int dec_pages_of(const DecodeParams &p, int b) {
-    const int len = p.seq_lens[b];
+    const int len = dec_len(p, b);
     return len > 0 ? (len + kDecPage - 1) / kDecPage - dec_first_token(p, b) / kDecPage : 0;
 }
 
@@ -221,7 +233,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 const bool valid = (unsigned)pid < (unsigned)p.num_pages;
                 DecodeStageMeta mt;
                 mt.b = b;
-                mt.ntok = valid ? (last_of_seq ? p.seq_lens[b] - (fp_b + lp) * kDecPage : kDecPage)
+                mt.ntok = valid ? (last_of_seq ? dec_len(p, b) - (fp_b + lp) * kDecPage : kDecPage)
                                 : 0;
                 mt.lo = lp == 0 ? dec_first_token(p, b) - fp_b * kDecPage : 0;
                 mt.first = (it == 0 || lp == 0) ? 1 : 0;
@@ -504,10 +516,13 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
 }
 
 // One CTA per sequence: combine the partial results of the CTAs that covered it.
+// A sequence whose length the page table cannot hold was treated as empty by the
+// split kernel; its CTA here records the error.
 __global__ void __launch_bounds__(256)
 decode_merge_kernel(const DecodeParams p, int G) {
     __shared__ long long red[2][8];
     const int b = blockIdx.x;
+    if (threadIdx.x == 0 && !dec_len_ok(p, b)) record_status(p.status, kStatusBounds);
     // start page of sequence b and total pages T
     long long before = 0, total = 0;
     for (int i = threadIdx.x; i < p.B; i += blockDim.x) {

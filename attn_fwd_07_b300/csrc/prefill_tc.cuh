@@ -129,6 +129,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     using C = PrefillCfg<D>;
     extern __shared__ uint8_t pf_smem_raw[];
 
+    // packed sequences: cu_seqlens must start at 0 and end at the total token count,
+    // or rows are left unwritten (checked once per launch)
+    if (p.cu_seqlens && blockIdx.x == 0 && threadIdx.x == 0 &&
+        (p.cu_seqlens[0] != 0 || p.cu_seqlens[p.nseq] != p.total))
+        record_status(p.status, kStatusBounds);
+
     // ---- work item: heaviest query tiles first, heads fastest (a key/value head's
     //      query heads run together and share its K/V tiles in L2)
     const int hunits = p.head_pairs ? p.Hq / 2 : p.Hq;
@@ -142,8 +148,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     int tok0, qlen, batch;
     if (p.cu_seqlens) {
         tok0 = p.cu_seqlens[sq];
-        qlen = p.cu_seqlens[sq + 1] - tok0;
+        const int tend = p.cu_seqlens[sq + 1];
+        qlen = tend - tok0;
         batch = 0;
+        // uniform: a sequence whose tokens leave [0, total) is skipped, nothing of it
+        // read or written; one longer than the launch's tiles has only those rows done
+        if (tok0 < 0 || tend < tok0 || tend > p.total) {
+            if (threadIdx.x == 0 && outer == nouter - 1 && hu == 0)
+                record_status(p.status, kStatusBounds);
+            return;
+        }
+        if (threadIdx.x == 0 && outer == nouter - 1 && hu == 0 &&
+            qlen > (p.tile0 + p.ntiles) * PrefillCfg<D>::BM)
+            record_status(p.status, kStatusBounds);
     } else {
         tok0 = 0;
         qlen = p.N;

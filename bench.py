@@ -253,6 +253,37 @@ def nbytes(*ts) -> int:
     return int(sum(t.numel() * t.element_size() for t in ts))
 
 
+def workload_shape(kind, w, spec):
+    """The workload's sizes as the JSON line's config reports them (both arms)."""
+    if kind in ("decode", "decode_fp8"):
+        B, Hq, d = w.q.shape
+        shape = {"B": B, "Hq": Hq, "Hkv": int(w.k_cache.shape[2]), "d": d,
+                 "page_size": int(w.k_cache.shape[1]), "total_tokens": int(w.seq_lens.sum())}
+    elif kind == "chunk":
+        T, Hq, d = w.q.shape
+        shape = {"seqs": len(w.q_lens), "total_q": T, "cached_tokens": int(w.seq_lens.sum()),
+                 "Hq": Hq, "Hkv": int(w.k_cache.shape[2]), "d": d, "causal": w.causal}
+    elif kind == "window":
+        B, N, Hq, d = w.q.shape
+        shape = {"B": B, "N": N, "Hq": Hq, "Hkv": int(w.k.shape[2]), "d": d,
+                 "window": list(w.window)}
+    elif kind == "varlen":
+        T, Hq, d = w.q.shape
+        shape = {"seqs": len(w.lens), "total_tokens": T, "Hq": Hq, "Hkv": int(w.k.shape[1]),
+                 "d": d, "causal": w.causal}
+    else:
+        B, N, Hq, d = w.q.shape
+        shape = {"B": B, "N": N, "Hq": Hq, "Hkv": int(w.k.shape[2]), "d": d,
+                 "causal": w.causal}
+    shape["values"] = spec.description
+    shape["name"] = spec.name
+    return shape
+
+
+def config_key(kind):
+    return "prefill" if kind == "dense" else kind
+
+
 class Leg:
     """One workload of the step: device-resident inputs, a launch, its algorithmic work,
     and an end-to-end variant that copies the inputs in from pinned host memory and the
@@ -277,15 +308,11 @@ class Leg:
             B, Hq, d = w.q.shape
             self.o = torch.empty_like(q)
             self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-            self.ws = torch.empty(A.attn_decode_workspace_size(B, Hq, kc.shape[2], d,
-                                                               w.page_table.shape[1],
+            self.ws = torch.empty(A.attn_decode_workspace_size(B, Hq, d, w.page_table.shape[1],
                                                                kc.shape[1]),
                                   dtype=torch.uint8, device=dev)
             self.work, self.unit, self.bound = decode_bytes(w), "GB/s", "hbm"
             self.kernel = "decode_split_kernel" + ("<true>" if self.kind == "decode_fp8" else "")
-            self.shape = {"B": B, "Hq": Hq, "Hkv": int(kc.shape[2]), "d": d,
-                          "page_size": int(kc.shape[1]),
-                          "total_tokens": int(w.seq_lens.sum())}
         else:
             if self.kind == "chunk":
                 self.host = [w.q, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.cu_seqlens_q]
@@ -298,31 +325,27 @@ class Leg:
                 T, Hq, d = w.q.shape
                 self.max_len = int(w.q_lens.max())
                 self.lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
-                self.shape = {"seqs": len(w.q_lens), "total_q": T,
-                              "cached_tokens": int(w.seq_lens.sum()), "Hq": Hq,
-                              "Hkv": int(w.k_cache.shape[2]), "d": d, "causal": w.causal}
-            elif self.kind == "window":
-                B, N, Hq, d = w.q.shape
-                self.lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-                self.shape = {"B": B, "N": N, "Hq": Hq, "Hkv": int(w.k.shape[2]), "d": d,
-                              "window": list(w.window)}
             elif self.kind == "varlen":
                 T, Hq, d = w.q.shape
                 self.max_len = int(w.lens.max())
                 self.lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
-                self.shape = {"seqs": len(w.lens), "total_tokens": T, "Hq": Hq,
-                              "Hkv": int(w.k.shape[1]), "d": d, "causal": w.causal}
             else:
                 B, N, Hq, d = w.q.shape
                 self.lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-                self.shape = {"B": B, "N": N, "Hq": Hq, "Hkv": int(w.k.shape[2]), "d": d,
-                              "causal": w.causal}
             self.f32 = w.q.dtype == torch.float32
             self.work, self.unit = prefill_flops(w), "TFLOP/s"
             self.bound = "alu" if self.f32 else "tensor"
             self.kernel = "prefill_simt_kernel" if self.f32 else "prefill_tc_kernel"
-        self.shape["values"] = self.spec.description
-        self.h2d = nbytes(*self.host)
+        self.shape = workload_shape(self.kind, w, self.spec)
+        # end to end: a decode step's query, page table and lengths come from the host and
+        # its O and LSE go back, while the cache stays resident on the device (where a
+        # serving process keeps it between steps); every other workload copies all of
+        # its inputs in
+        self.e2e_in = ([0, 3, 4] if self.kind in ("decode", "decode_fp8")
+                       else list(range(len(self.host))))
+        self.resident = (nbytes(*[t for i, t in enumerate(self.host) if i not in self.e2e_in])
+                         if self.kind in ("decode", "decode_fp8") else 0)
+        self.h2d = nbytes(*[self.host[i] for i in self.e2e_in])
         self.d2h = nbytes(self.o, self.lse)
 
     def launch(self, stream):
@@ -358,7 +381,7 @@ class Leg:
         return work / (ms * 1e-3) / (1e12 if self.unit == "TFLOP/s" else 1e9)
 
     def e2e_setup(self):
-        self.h_in = [t.pin_memory() for t in self.host]
+        self.h_in = {i: self.host[i].pin_memory() for i in self.e2e_in}
         self.h_out = [torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory(),
                       torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()]
 
@@ -370,8 +393,8 @@ class Leg:
             self.A.attn_fwd_host(self.h_in[0], self.h_in[1], self.h_in[2], self.w.causal,
                                  self.scale, o=self.h_out[0], lse=self.h_out[1], stream=stream)
             return
-        for dst, src in zip(self.dev, self.h_in):
-            dst.copy_(src, non_blocking=True)
+        for i, src in self.h_in.items():
+            self.dev[i].copy_(src, non_blocking=True)
         self.launch(stream)
         self.h_out[0].copy_(self.o, non_blocking=True)
         self.h_out[1].copy_(self.lse, non_blocking=True)
@@ -512,9 +535,11 @@ def run_reference(args):
     # gets an equal share, and a sample always completes at least one batch of rows
     per_step = args.ref_seconds / max(1, args.steps) / len(names)
     results = []
+    shapes = {}
     for name in names:
         kind = inputs.WORKLOADS[name].kind
         w = inputs.make(name, args.batch)
+        shapes[config_key(kind)] = workload_shape(kind, w, inputs.WORKLOADS[name])
         for _ in range(args.warmup):
             cpu_oracle_sample(w, kind, 0.05)
         vals, els, descs, cores = [], 0.0, [], 0
@@ -532,8 +557,9 @@ def run_reference(args):
         "ms_per_step": 1000.0 * sum(r[4] for r in results) / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": " + ".join(names), "batch_override": args.batch,
-                   "parallelism": "single process", "l2": "not applicable (CPU)"},
+        "config": dict({"workload": " + ".join(names), "batch_override": args.batch,
+                        "parallelism": "single process", "l2": "not applicable (CPU)"},
+                       **shapes),
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": "per step: %s; %d steps" % (desc, args.steps)},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
@@ -650,9 +676,12 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize(dev)
         ms = max_over_ranks(a.elapsed_time(b), world, dev)
-        e2e.append({"value": leg.rate(sum_over_ranks(leg.work * n_e2e, world, dev), ms),
-                    "unit": leg.unit, "h2d_bytes_per_step": leg.h2d,
-                    "d2h_bytes_per_step": leg.d2h})
+        rec = {"value": leg.rate(sum_over_ranks(leg.work * n_e2e, world, dev), ms),
+               "unit": leg.unit, "h2d_bytes_per_step": leg.h2d, "d2h_bytes_per_step": leg.d2h}
+        if leg.resident:
+            rec["resident_bytes"] = leg.resident
+            rec["resident"] = "KV cache kept on the device between steps"
+        e2e.append(rec)
         leg.e2e_teardown()
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, one GPU only)
@@ -671,8 +700,7 @@ def run_gpu(args):
         config = {"workload": " + ".join(names), "batch_override": args.batch,
                   "parallelism": "replicas" if world > 1 else "single GPU", "l2": l2}
         for leg in legs:
-            config[leg.kind if leg.kind != "dense" else "prefill"] = dict(leg.shape,
-                                                                           name=leg.name)
+            config[config_key(leg.kind)] = dict(leg.shape)
         line = {
             "metric": METRIC, "value": leg_val[0], "unit": p0.unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,

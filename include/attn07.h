@@ -35,10 +35,14 @@
  *   - Invalid arguments return ATTN_ERR_INVALID_ARG and launch nothing;
  *     sizes outside what the kernels implement return ATTN_ERR_UNSUPPORTED and
  *     launch nothing.  Launch failures return ATTN_ERR_CUDA.
- *   - Errors found on the device (a page id out of range; a pipeline wait that
- *     ran past its bound) never fault the device: the kernel records them in a
- *     device status word, skips the access, and
- *     attn_get_device_status() reports them.
+ *   - `scale` must be finite and > 0 (1/sqrt(d) in the usual case); any other
+ *     value returns ATTN_ERR_INVALID_ARG.
+ *   - Errors found on the device never fault the device: the kernel records
+ *     them in a device status word, skips the access, and
+ *     attn_get_device_status() reports them.  They are: a page id out of
+ *     range, a sequence length outside what the page table can hold, a
+ *     cu_seqlens vector that breaks its rules (ATTN_ERR_DEVICE_BOUNDS), and a
+ *     pipeline wait that ran past its bound (ATTN_ERR_TIMEOUT).
  *   - Entry points are thread-safe and re-entrant.
  *   - bf16 means IEEE bfloat16 (1-8-7) stored in 2 bytes, round-to-nearest-even
  *     on output.
@@ -62,7 +66,7 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, page size, ...) */
     ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
     ATTN_ERR_TIMEOUT = 4,      /* a device-side pipeline wait ran past its bound */
-    ATTN_ERR_DEVICE_BOUNDS = 5 /* the device found an index out of range (page id) */
+    ATTN_ERR_DEVICE_BOUNDS = 5 /* the device found an index or length out of range */
 } attn_status_t;
 
 /*
@@ -167,8 +171,9 @@ attn_status_t attn_fwd_two_pass(const void *q, const void *k, const void *v, voi
  *                seq_lens[s] - q_len + i.  Needs q_len <= seq_lens[s] <=
  *                max_pages_per_seq * page_size; a sequence that breaks this is
  *                skipped and ATTN_ERR_DEVICE_BOUNDS recorded.
- *   cu_seqlens_q int32 [num_seqs + 1], DEVICE (as attn_fwd_varlen); max_qlen a
- *                host-side bound on every q_len.
+ *   cu_seqlens_q int32 [num_seqs + 1], DEVICE, with the rules and device checks
+ *                of attn_fwd_varlen's cu_seqlens (over total_q tokens); max_qlen
+ *                a host-side bound on every q_len, checked as max_seqlen is.
  *   o            [total_q, Hq, d] bf16;  lse [Hq, total_q] fp32 or NULL.
  *   causal != 0: query i sees positions <= its own; else all cached tokens.
  *   A page id out of range is recorded as ATTN_ERR_DEVICE_BOUNDS and its tokens
@@ -183,25 +188,41 @@ attn_status_t attn_fwd_chunked_paged(const void *q, const void *k_cache, const v
                                      int causal, float scale, attn_stream_t stream);
 
 /*
- * attn_fwd_f32 -- the same operation with fp32 q, k, v and o (same layouts and
- * rules as attn_fwd).  Arithmetic is fp32 throughout (no reduced-precision
- * tensor-core path).  1 <= d <= 128 and d % 4 == 0.
+ * attn_fwd_f32 -- the same operation with fp32 q, k, v and o: the attention
+ * formula of the fatihsoysal.com page, section "Transformer Mimarisi ve
+ * Self-Attention Mekanizması", in its plain form where Q, K and V are each a
+ * (sequence length, dimension) matrix of real numbers, computed tile by tile
+ * with the online softmax of section "Online Softmax Prensibi".  Arithmetic is
+ * fp32 throughout, on the CUDA cores (no reduced-precision tensor-core path).
+ * Same layouts and rules as attn_fwd, except the head dimension:
+ * 16 <= d <= 128 and d % 16 == 0 (else ATTN_ERR_UNSUPPORTED).  B <= 65535 and
+ * Hq <= 65535.
  */
 attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float *o,
                            float *lse, int B, int Hq, int Hkv, int N, int d, int causal,
                            float scale, attn_stream_t stream);
 
 /*
- * attn_fwd_varlen -- prefill over sequences of different lengths packed along
- * the token axis; each sequence is an independent attention problem.
+ * attn_fwd_varlen -- prefill over a batch of requests of different lengths
+ * (yapayzekasozluk.tr "attention" tag page, entry "KV Cache": batched inference
+ * serves requests of different lengths together), packed along the token axis
+ * with no padding.  Each sequence is an independent problem of the attention
+ * formula (fatihsoysal.com page, section "Transformer Mimarisi ve
+ * Self-Attention Mekanizması"), computed as in attn_fwd.
  *   q   [total_tokens, Hq,  d] bf16      k,v [total_tokens, Hkv, d] bf16
  *   o   [total_tokens, Hq,  d] bf16      lse [Hq, total_tokens] fp32 or NULL
  *   cu_seqlens  int32 [num_seqs + 1], DEVICE pointer: sequence s owns tokens
  *               cu_seqlens[s] .. cu_seqlens[s+1]-1; cu_seqlens[0] = 0,
  *               non-decreasing, cu_seqlens[num_seqs] = total_tokens.
  *   max_seqlen  host-side upper bound on every sequence length (sizes the
- *               launch; a sequence longer than it is not fully computed).
+ *               launch).
  *   Zero-length sequences are allowed.  d must be 64 or 128.
+ *   Checked on the device, each recording ATTN_ERR_DEVICE_BOUNDS: a sequence
+ *   whose tokens leave [0, total_tokens) or whose length is negative is skipped
+ *   (nothing of it is read or written); a sequence longer than the launch's
+ *   query tiles (ceil(max_seqlen / 128) tiles of 128 rows) has only the rows
+ *   of those tiles written; cu_seqlens[0] != 0 or cu_seqlens[num_seqs] !=
+ *   total_tokens leaves the rows outside the sequences unwritten.
  */
 attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                               const int32_t *cu_seqlens, int num_seqs, int total_tokens,
@@ -225,6 +246,9 @@ attn_status_t attn_fwd_varlen(const void *q, const void *k, const void *v, void 
  *               only the first ceil(seq_lens[b]/page_size) entries are read.
  *   seq_lens    int32 [B]: cached tokens per sequence, 0 <= seq_lens[b] <=
  *               max_pages_per_seq * page_size.  DEVICE pointer (read on the device).
+ *               A sequence outside that range is treated as empty (its page
+ *               table row is not read; O = 0, LSE = -inf) and
+ *               ATTN_ERR_DEVICE_BOUNDS is recorded.
  *   o           [B, Hq, d] bf16, written;  lse [B, Hq] fp32 or NULL.
  *   workspace   device scratch of at least attn_decode_workspace_size(...) bytes,
  *               16-byte aligned, owned by the caller; its contents on entry do
@@ -286,12 +310,13 @@ attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const
                                        size_t workspace_bytes, attn_stream_t stream);
 
 /*
- * Bytes of workspace attn_decode_paged needs for these sizes (0 on invalid
- * sizes).  It depends only on B, Hq, d and the GPU's SM count, never on the
- * sequence lengths.
+ * Bytes of workspace attn_decode_paged (and attn_decode_paged_window,
+ * attn_decode_paged_fp8) needs for these sizes on the current device: the
+ * partial outputs and log-sum-exps of the split key ranges (fp32).  0 on
+ * invalid sizes or when the device cannot be queried.  It depends only on B,
+ * Hq, d and the GPU's SM count, never on the sequence lengths.
  */
-size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int max_pages_per_seq,
-                                  int page_size);
+size_t attn_decode_workspace_size(int B, int Hq, int d, int max_pages_per_seq, int page_size);
 
 /* Static, human-readable text for a status code. */
 const char *attn_status_string(attn_status_t s);

@@ -36,3 +36,27 @@ def assert_close(e, what=""):
     assert e["mean_o"] <= TOL_MEAN_O, (what, e)
     if "max_lse" in e:
         assert e["max_lse"] <= TOL_MAX_LSE, (what, e)
+
+
+# |dO| histogram bin edges for the full-output reports
+HIST_EDGES = (0.0, 1e-4, 3e-4, 1e-3, 3e-3, 1e-2, np.inf)
+
+# reports of the full-output comparisons, printed at the end of the run (conftest)
+REPORTS = []
+
+
+def full_report(name, o_gpu, o_ref, lse_gpu, lse_ref, row_axes):
+    """Error figures over every output element of a workload: max and mean |dO|, the
+    worst row (its index along `row_axes` of O), max |dLSE| and a histogram of |dO|.
+    The report is kept for the end-of-run summary and returned."""
+    e = errors(o_gpu, o_ref, lse_gpu, lse_ref)
+    d = np.abs(np.asarray(o_gpu, np.float64) - np.asarray(o_ref, np.float64))
+    hist, _ = np.histogram(d, bins=np.array(HIST_EDGES))
+    rep = {"workload": name, "elements": int(d.size), "max_o": e["max_o"],
+           "mean_o": e["mean_o"], "max_lse": e["max_lse"],
+           "worst_row": [int(e["worst_o_index"][a]) for a in row_axes],
+           "hist_edges": [float(x) for x in HIST_EDGES[1:-1]],
+           "hist_counts": [int(c) for c in hist]}
+    REPORTS.append(rep)
+    return e, rep
+

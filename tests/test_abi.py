@@ -11,6 +11,7 @@ from attn_fwd_07_b300 import build as B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "attn07.h")
+TEST_HEADER = os.path.join(ROOT, "include", "attn07_testing.h")
 
 
 @pytest.fixture(scope="module")
@@ -19,8 +20,8 @@ def lib():
     return A.load_library()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(path=HEADER):
+    text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", text)))
 
@@ -33,8 +34,14 @@ def test_header_declares_the_boundary():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    for name in declared_functions():
+    for name in declared_functions() + declared_functions(TEST_HEADER):
         assert hasattr(lib, name), name
+
+
+def test_test_hooks_stay_out_of_the_interface():
+    hooks = declared_functions(TEST_HEADER)
+    assert hooks == ["attn_testing_decode_paged_ctas"]
+    assert not set(hooks) & set(declared_functions())
 
 
 def test_status_strings(lib):
@@ -88,7 +95,33 @@ def test_varlen_and_decode_validation(lib):
     many_kv = list(args)       # 16 key/value heads: one consumer warp each would exceed 8
     many_kv[8], many_kv[9] = 32, 16
     assert lib.attn_decode_paged(*many_kv, p, 1 << 30, None) == A.ATTN_ERR_UNSUPPORTED
-    assert lib.attn_decode_workspace_size(0, 32, 8, 128, 10, 16) == 0
+    assert lib.attn_decode_workspace_size(0, 32, 128, 10, 16) == 0
+    # the scale rule is the same for every entry point: finite and > 0
+    for bad in (0.0, -0.1, float("inf"), float("nan")):
+        assert lib.attn_decode_paged(*args[:-1], bad, p, 1 << 30, None) == A.ATTN_ERR_INVALID_ARG
+        assert lib.attn_fwd_f32(p, p, p, p, None, 1, 1, 1, 8, 64, 1, bad,
+                                None) == A.ATTN_ERR_INVALID_ARG
+        assert lib.attn_fwd_varlen(p, p, p, p, None, p, 2, 10, 8, 4, 2, 128, 1, bad,
+                                   None) == A.ATTN_ERR_INVALID_ARG
+
+
+def test_f32_head_dim_rule(lib):
+    """attn_fwd_f32 implements 16 <= d <= 128 with d % 16 == 0, as its header states."""
+    P = ctypes.c_void_p
+    p = P(1 << 20)
+    for d in (8, 24, 100, 144, 256):
+        assert lib.attn_fwd_f32(p, p, p, p, None, 1, 1, 1, 8, d, 1, 0.1,
+                                None) == A.ATTN_ERR_UNSUPPORTED, d
+    text = open(HEADER).read()
+    assert "16 <= d <= 128 and d % 16 == 0" in text
+
+
+def test_workspace_size_signature():
+    """attn_decode_workspace_size(B, Hq, d, max_pages_per_seq, page_size): five sizes."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    m = re.search(r"attn_decode_workspace_size\(([^)]*)\)", text)
+    names = [a.split()[-1] for a in m.group(1).split(",")]
+    assert names == ["B", "Hq", "d", "max_pages_per_seq", "page_size"]
 
 
 def test_host_entry_validation(lib):

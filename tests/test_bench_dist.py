@@ -129,3 +129,8 @@ def test_reference_arm_prints_one_contract_line():
     assert d["vs_baseline"] is None
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    # the config names the workload's sizes exactly as the GPU arm's line does
+    from attn_fwd_07_b300 import inputs
+    spec = inputs.WORKLOADS["single_head_f32"]
+    assert d["config"]["prefill"] == bench.workload_shape(spec.kind, inputs.make(spec.name),
+                                                          spec)

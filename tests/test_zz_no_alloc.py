@@ -46,7 +46,7 @@ def test_noalloc_decode_rejects_sizes_beyond_its_scratch():
         pytest.skip("no CUDA device")
     lib = A.load_library()
     B, Hq, Hkv, d = 4096, 64, 8, 128   # needs far more than the built-in scratch
-    assert A.attn_decode_workspace_size(B, Hq, Hkv, d, 8, 16) > (8 << 20)
+    assert A.attn_decode_workspace_size(B, Hq, d, 8, 16) > (8 << 20)
     p = torch.empty(16, dtype=torch.uint8, device="cuda")
     ptr = p.data_ptr()
     import ctypes
