@@ -217,11 +217,12 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     p.kv_lens = paged ? paged->kv_lens : nullptr;
     p.maxp = paged ? paged->maxp : 0;
     p.num_pages = paged ? paged->num_pages : 0;
-    const long long grid = p.head_pairs ? (long long)ntiles * (Hq / 2) * nseq
-                                        : (long long)((ntiles + 1) / 2) * Hq * nseq;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-    if (grid == 0) return ATTN_OK;
-    const unsigned gx = (unsigned)grid;
+    // work items (pairs of query tiles); persistent CTAs, one per SM, walk them
+    const long long items = p.head_pairs ? (long long)ntiles * (Hq / 2) * nseq
+                                         : (long long)((ntiles + 1) / 2) * Hq * nseq;
+    if (items > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+    if (items == 0) return ATTN_OK;
+    const unsigned gx = (unsigned)std::min<long long>(items, st->sms);
     if (d == 128)
         launch_prefill_variant<128>(gx, p, mq, mk, mv, paged != nullptr, pass, stream);
     else
@@ -485,7 +486,21 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     else
         decode_split_kernel<false><<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
     if ((s = launch_status()) != ATTN_OK) return s;
-    decode_merge_kernel<<<B, 256, 0, cs>>>(p, G);
+    // the merge as a programmatic dependent of the split kernel: it is scheduled while
+    // the split kernel's last CTAs run and waits on the device for their results, which
+    // takes the launch gap between the two kernels off the step
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((Hq + 7) / 8), (unsigned)B, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, p, G);
+    if (e != cudaSuccess) return cuda_fail(e);
     return launch_status();
 }
 

@@ -154,6 +154,8 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
     const int lane = threadIdx.x & 31;
     const int Hkv = p.Hkv;
     const int G = gridDim.x;
+    // the merge grid may be scheduled now (it waits for this grid to finish)
+    grid_dependents_launch();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -515,17 +517,25 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
     __syncthreads();
 }
 
-// One CTA per sequence: combine the partial results of the CTAs that covered it.
+// One warp per (sequence b, query head h): combine the partial results of the CTAs
+// that covered the sequence by their log-sum-exps, lanes splitting the partials
+// (for the maximum and the weights) and then the d dimensions (for the weighted
+// sum).  Grid (ceil(Hq / 8), B), 256 threads.  Launched as a programmatic
+// dependent of the split kernel, so it may start while the split kernel's last CTAs
+// still run: it waits for that grid's completion before reading the partials.
 // A sequence whose length the page table cannot hold was treated as empty by the
-// split kernel; its CTA here records the error.
+// split kernel; this kernel records the error, once per sequence.
 __global__ void __launch_bounds__(256)
 decode_merge_kernel(const DecodeParams p, int G) {
-    __shared__ long long red[2][8];
-    const int b = blockIdx.x;
-    if (threadIdx.x == 0 && !dec_len_ok(p, b)) record_status(p.status, kStatusBounds);
+    grid_dependency_wait();
+    const int b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x * 8 + warp;
+    if (h >= p.Hq) return;
+    if (h == 0 && lane == 0 && !dec_len_ok(p, b)) record_status(p.status, kStatusBounds);
     // start page of sequence b and total pages T
     long long before = 0, total = 0;
-    for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+    for (int i = lane; i < p.B; i += 32) {
         const int np = dec_pages_of(p, i);
         total += np;
         if (i < b) before += np;
@@ -535,63 +545,59 @@ decode_merge_kernel(const DecodeParams p, int G) {
         before += __shfl_xor_sync(0xffffffffu, before, o);
         total += __shfl_xor_sync(0xffffffffu, total, o);
     }
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        red[0][warp] = before;
-        red[1][warp] = total;
-    }
-    __syncthreads();
-    before = 0;
-    total = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-        before += red[0][w];
-        total += red[1][w];
-    }
     const int np = dec_pages_of(p, b);
-    const int dq = p.d / 4;
-    if (np == 0) {
-        for (int idx = threadIdx.x; idx < p.Hq * dq; idx += blockDim.x) {
-            const int h = idx / dq, c = (idx % dq) * 4;
-            __nv_bfloat16 *ob = p.o + ((long long)b * p.Hq + h) * p.d + c;
-            *reinterpret_cast<uint2 *>(ob) = make_uint2(0u, 0u);
-            if (p.lse && c == 0) p.lse[(long long)b * p.Hq + h] = -INFINITY;
-        }
-        return;
-    }
-    const int c0 = dec_cta_of_page(before, total, G);
-    const int c1 = dec_cta_of_page(before + np - 1, total, G);
-    for (int idx = threadIdx.x; idx < p.Hq * dq; idx += blockDim.x) {
-        const int h = idx / dq, c = (idx % dq) * 4;
+    const int dpl = p.d / 32;  // dimensions per lane: 2 or 4
+    __nv_bfloat16 *ob = p.o + ((long long)b * p.Hq + h) * p.d + lane * dpl;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float mx = -INFINITY, wsum = 0.f;
+    if (np > 0) {
         // CTAs c0..c1 cover the sequence's pages; a CTA whose range is empty (more CTAs
         // than pages) wrote nothing and is skipped
-        float mx = -INFINITY;
-        for (int cc = c0; cc <= c1; ++cc)
+        const int c0 = dec_cta_of_page(before, total, G);
+        const int c1 = dec_cta_of_page(before + np - 1, total, G);
+        for (int cc = c0 + lane; cc <= c1; cc += 32)
             if (dec_range_nonempty(cc, total, G))
                 mx = fmaxf(mx, p.part_lse[((long long)b + cc) * p.Hq + h]);
-        float wsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (mx != -INFINITY) {
-            for (int cc = c0; cc <= c1; ++cc) {
-                if (!dec_range_nonempty(cc, total, G)) continue;
-                const long long slot = (long long)b + cc;
-                const float ls = p.part_lse[slot * p.Hq + h];
-                const float w = ex2((ls - mx) * kLog2e);
+            for (int cb = c0; cb <= c1; cb += 32) {
+                const int cc = cb + lane;
+                float w = 0.f;
+                if (cc <= c1 && dec_range_nonempty(cc, total, G))
+                    w = ex2((p.part_lse[((long long)b + cc) * p.Hq + h] - mx) * kLog2e);
                 wsum += w;
-                const float4 po =
-                    *reinterpret_cast<const float4 *>(p.part_o + (slot * p.Hq + h) * p.d + c);
-                acc.x = fmaf(w, po.x, acc.x);
-                acc.y = fmaf(w, po.y, acc.y);
-                acc.z = fmaf(w, po.z, acc.z);
-                acc.w = fmaf(w, po.w, acc.w);
+                const int n = min(32, c1 - cb + 1);
+                for (int i = 0; i < n; ++i) {
+                    const float wi = __shfl_sync(0xffffffffu, w, i);
+                    if (wi == 0.f) continue;  // same for every lane
+                    const float *po = p.part_o + (((long long)b + cb + i) * p.Hq + h) * p.d +
+                                      lane * dpl;
+                    if (dpl == 4) {
+                        const float4 v = *reinterpret_cast<const float4 *>(po);
+                        acc[0] = fmaf(wi, v.x, acc[0]);
+                        acc[1] = fmaf(wi, v.y, acc[1]);
+                        acc[2] = fmaf(wi, v.z, acc[2]);
+                        acc[3] = fmaf(wi, v.w, acc[3]);
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2 *>(po);
+                        acc[0] = fmaf(wi, v.x, acc[0]);
+                        acc[1] = fmaf(wi, v.y, acc[1]);
+                    }
+                }
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
         }
-        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-        __nv_bfloat16 *ob = p.o + ((long long)b * p.Hq + h) * p.d + c;
-        *reinterpret_cast<uint2 *>(ob) =
-            make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
-        if (p.lse && c == 0)
-            p.lse[(long long)b * p.Hq + h] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
     }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    if (dpl == 4)
+        *reinterpret_cast<uint2 *>(ob) = make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv),
+                                                    pack_bf16(acc[2] * inv, acc[3] * inv));
+    else
+        *reinterpret_cast<uint32_t *>(ob) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    if (p.lse && lane == 0)
+        p.lse[(long long)b * p.Hq + h] = wsum > 0.f ? mx + __logf(wsum) : -INFINITY;
 }
 
 }  // namespace attn07

@@ -11,35 +11,48 @@
 // that each stream all the keys and values they need, loading the next block
 // while the current one is computed.
 //
-// One CTA owns two 128-row query tiles that share one key/value head: two
-// query heads of the same group on the same rows when the group size is even,
-// else two consecutive row tiles of one head.  Both tiles use every K_j and
-// V_j tile loaded into shared memory, which halves the load traffic per MMA,
-// and the two tiles' softmax runs while the tensor core works on the other
-// tile ("ping-pong").
+// Work item: two 128-row query tiles that share one key/value head -- two query
+// heads of the same group on the same rows when the group size is even, else
+// two consecutive row tiles of one head.  Both tiles use every K_j and V_j tile
+// loaded into shared memory, which halves the load traffic per MMA, and the
+// two tiles' softmax runs while the tensor core works on the other tile
+// ("ping-pong").
 //
-// Warp roles (384 threads):
-//   warps 0-3   softmax of tile 0, one thread per query row (TMEM lane)
-//   warps 4-7   softmax of tile 1
-//   warp 8      TMA producer: both Q tiles once, then K_j / V_j (128 keys)
-//               into two shared-memory rings (128-byte swizzle)
-//   warp 9      MMA issuer (one thread), in this order for every j (PV with N = d
-//               in one instruction per 16 keys: M128 N64 instructions run at about
-//               70% of the tensor core's rate, N128 at full rate):
-//                  O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,
-//                  O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
-//               tcgen05.mma ops of one thread execute in issue order, so
-//               S_{j+1} never overwrites P_j before O += P_j V_j has read it,
-//               and a commit after S_{j+1} also covers that PV product.
-//   warps 10-11 idle (they complete the third warpgroup)
+// Persistent CTAs: one CTA per SM walks the items, round r taking item
+// r * gridDim.x + c (c = blockIdx.x; the order reverses every other round, which
+// evens out the heaviest-first list of causal items).  Each role keeps its own
+// position in the stream of items, so the next item's query tiles and first key
+// tiles load, and its first products run, while the previous item's output is
+// still being written: the per-item costs of a launch (set-up, first loads,
+// epilogue) are paid once per CTA.
+//
+// Warp roles (512 threads, four warpgroups):
+//   warps 0-3    softmax of tile 0, one thread per query row (TMEM lane)
+//   warps 4-7    softmax of tile 1
+//   warps 8-11   epilogue: O / L -> bf16 rows in device memory, for both tiles
+//   warp 12      TMA producer: both Q tiles of an item, then K_j / V_j (128
+//                keys) into two shared-memory rings (128-byte swizzle)
+//   warp 13      MMA issuer (one thread), in this order for every j (PV with
+//                N = d in one instruction per 16 keys: M128 N64 instructions run
+//                at about 70% of the tensor core's rate, N128 at full rate):
+//                   O_0 += P_0 V_j,  S_0 = Q_0 K_{j+1}^T,
+//                   O_1 += P_1 V_j,  S_1 = Q_1 K_{j+1}^T
+//                tcgen05.mma ops of one thread execute in issue order, so
+//                S_{j+1} never overwrites P_j before O += P_j V_j has read it,
+//                and a commit after S_{j+1} also covers that PV product.
+//   warps 14-15  idle (they complete the fourth warpgroup)
+// The softmax warpgroups raise their register count to 192 per thread; the
+// other two lower theirs to 64 (192 + 64 = twice the 128 of the launch).
 //
 // Softmax step for tile t and key tile j (thread = row): load the S row from
-// TMEM, mask (causal diagonal / sequence end), running maximum, P = 2^(S *
-// scale * log2e - M) rounded to bf16 and written back over the S columns it
-// came from (P is the A operand of the PV product, read from TMEM), row sums.
-// After a row's first key tile the maximum is first skipped: P is taken against
-// the standing reference M, and only if some row's P sums past 2^24 on this tile
-// is the S row reloaded and the step redone with its maximum.
+// TMEM, mask (causal diagonal / window / sequence end), running maximum, P =
+// 2^(S * scale * log2e - M) rounded to bf16 and written back over the S
+// columns it came from (P is the A operand of the PV product, read from TMEM),
+// row sums.  After a row's first key tile the maximum is first skipped: P is
+// taken against the standing reference M, and only if some row's P sums past
+// 2^24 on this tile is the S row reloaded and the step redone with its maximum.
+// At the end of an item the softmax writes the row's LSE and hands 1 / L to the
+// epilogue through shared memory.
 //
 // Rescaling: the row maximum used in the exponent only moves when the new
 // maximum exceeds it by more than 8 (log2 units).  Until then P may reach
@@ -51,6 +64,8 @@
 // Tensor memory (512 columns of 128 lanes x 32 bit):
 //   [0,128) S_0 (P_0 in its first 64 columns), [128,256) S_1 / P_1,
 //   [256,256+d) O_0, [384,384+d) O_1
+// The first PV product of an item into O_t waits until the epilogue has read
+// the previous item's O_t out of TMEM.
 #pragma once
 
 #include "ptx.cuh"
@@ -68,7 +83,7 @@ struct PrefillParams {
     int Hq, Hkv;
     int ntiles;     // 128-row query tiles per sequence (of the longest sequence) to run
     int tile0;      // the first of them: tiles [tile0, tile0 + ntiles) of each sequence
-    int head_pairs; // 1: a CTA takes two heads of a group on the same rows; 0: two row tiles
+    int head_pairs; // 1: an item takes two heads of a group on the same rows; 0: two row tiles
     int wl, wr;     // query i sees keys i - wl .. i + wr; -1: no limit on that side
                     // (causal: wl = -1, wr = 0; full: wl = wr = -1)
     float scale_log2;
@@ -91,27 +106,143 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_Q = 0;                  // Q_0, Q_1
     static constexpr uint32_t OFF_K = 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + SK * TILE;
-    static constexpr uint32_t OFF_CTRL = OFF_V + SV * TILE;
+    static constexpr uint32_t OFF_STATS = OFF_V + SV * TILE;  // [2][128] fp32: 1 / L per row
+    static constexpr uint32_t OFF_CTRL = OFF_STATS + 2 * 128 * 4;
     static constexpr uint32_t CTRL_BYTES = 512;
     static constexpr size_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
     // TMEM columns
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
-    static constexpr int THREADS = 384;
+    static constexpr int THREADS = 512;
+    // per-thread registers after the split: softmax warpgroups / the other two
+    static constexpr uint32_t REG_SOFTMAX = 192, REG_OTHER = 64;
 };
+
+static_assert(PrefillCfg<128>::SMEM <= 227 * 1024, "prefill shared memory");
+// four warpgroups of 128 threads share the 65536 registers the launch reserves
+static_assert(128 * (2 * PrefillCfg<128>::REG_SOFTMAX + 2 * PrefillCfg<128>::REG_OTHER) == 65536,
+              "register split must add up to the launch's registers");
 
 // barrier slots inside the control block (8 bytes each)
 enum : uint32_t {
-    BAR_Q = 0,
-    BAR_KFULL = 1,    // +s, s < 4
-    BAR_KEMPTY = 5,   // +s
-    BAR_VFULL = 9,    // +s
-    BAR_VEMPTY = 13,  // +s
-    BAR_SFULL = 17,   // +t, t < 2
-    BAR_PFULL = 19,   // +t
-    BAR_OFULL = 21,   // +t
-    BAR_DRAIN = 23,
-    BAR_COUNT = 24
+    BAR_QFULL = 0,
+    BAR_QEMPTY = 1,
+    BAR_KFULL = 2,    // +s, s < 4
+    BAR_KEMPTY = 6,   // +s
+    BAR_VFULL = 10,   // +s
+    BAR_VEMPTY = 14,  // +s
+    BAR_SFULL = 18,   // +t, t < 2
+    BAR_PFULL = 20,   // +t
+    BAR_OFULL = 22,   // +t
+    BAR_OEMPTY = 24,  // +t
+    BAR_STATS = 26,   // +t: 1 / L of the item's rows written
+    BAR_STATSE = 28,  // +t: ... and read by the epilogue
+    BAR_DRAIN = 30,
+    BAR_COUNT = 31
 };
+
+// One work item: the two query tiles, their rows, and the key tiles each needs.
+struct PrefillItem {
+    int head[2], row0[2], jlo[2], jhi[2];
+    bool valid[2];
+    int tok0, qlen, batch, kvlen, qoff, g, sq;
+    int J0, n_kv;  // key tiles J0 .. J0 + n_kv - 1 cover both tiles
+};
+
+__device__ __forceinline__ int prefill_items(const PrefillParams &p) {
+    const int units = (p.head_pairs ? p.Hq / 2 : p.Hq) * p.nseq;
+    const int nouter = p.head_pairs ? p.ntiles : (p.ntiles + 1) / 2;
+    return nouter * units;
+}
+
+// Item of round r for this CTA: forward in even rounds, backward in odd ones.
+__device__ __forceinline__ int prefill_item_index(int r) {
+    const int G = (int)gridDim.x;
+    return r * G + ((r & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+}
+
+// Decode item idx (heaviest query tiles first, heads fastest: a key/value head's
+// query heads run together and share its K/V tiles in L2).  Returns false when it
+// has nothing to compute.  With `report`, records the bounds errors it finds (one
+// role reports, so that each is recorded once).
+template <int D, bool PAGED>
+__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int idx, bool report,
+                                             PrefillItem &it) {
+    using C = PrefillCfg<D>;
+    const int hunits = p.head_pairs ? p.Hq / 2 : p.Hq;
+    const int units = hunits * p.nseq;
+    const int nouter = p.head_pairs ? p.ntiles : (p.ntiles + 1) / 2;
+    const int outer = nouter - 1 - idx / units;
+    const int rem = idx % units;
+    const int hu = rem % hunits;
+    const int sq = rem / hunits;
+    const bool seq_first = outer == nouter - 1 && hu == 0;  // one item per sequence
+    // query rows [0, qlen) of this sequence sit at positions qoff + i; keys at [0, kvlen)
+    int tok0, qlen, batch;
+    if (p.cu_seqlens) {
+        tok0 = p.cu_seqlens[sq];
+        const int tend = p.cu_seqlens[sq + 1];
+        qlen = tend - tok0;
+        batch = 0;
+        // a sequence whose tokens leave [0, total) is skipped, nothing of it read or
+        // written; one longer than the launch's tiles has only those rows done
+        if (tok0 < 0 || tend < tok0 || tend > p.total) {
+            if (report && seq_first) record_status(p.status, kStatusBounds);
+            return false;
+        }
+        if (report && seq_first && qlen > (p.tile0 + p.ntiles) * C::BM)
+            record_status(p.status, kStatusBounds);
+    } else {
+        tok0 = 0;
+        qlen = p.N;
+        batch = sq;
+    }
+    int kvlen = qlen, qoff = 0;
+    if constexpr (PAGED) {
+        kvlen = p.kv_lens[sq];
+        qoff = kvlen - qlen;
+        if (qoff < 0 || kvlen > p.maxp * 16) {  // the sequence's sizes are invalid
+            if (report && outer == nouter - 1 && qlen > 0) record_status(p.status, kStatusBounds);
+            return false;
+        }
+    }
+    if (p.head_pairs) {
+        it.head[0] = 2 * hu;
+        it.head[1] = 2 * hu + 1;
+        it.row0[0] = it.row0[1] = (p.tile0 + outer) * C::BM;
+    } else {
+        it.head[0] = it.head[1] = hu;
+        it.row0[0] = (p.tile0 + 2 * outer) * C::BM;
+        it.row0[1] = it.row0[0] + C::BM;
+    }
+    const int row_end = min(qlen, (p.tile0 + p.ntiles) * C::BM);  // rows this launch runs
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        it.valid[t] = it.row0[t] < row_end;
+        const int last_row = min(it.row0[t] + C::BM, qlen) - 1;
+        const int lo_key = p.wl < 0 ? 0 : max(0, qoff + it.row0[t] - p.wl);
+        const int hi_key = p.wr < 0 ? kvlen - 1 : min(kvlen - 1, qoff + last_row + p.wr);
+        it.jlo[t] = lo_key / C::BN;
+        it.jhi[t] = hi_key / C::BN;
+    }
+    if (!it.valid[0] && !it.valid[1]) return false;
+    it.J0 = it.valid[0] ? (it.valid[1] ? min(it.jlo[0], it.jlo[1]) : it.jlo[0]) : it.jlo[1];
+    const int J1 = it.valid[0] ? (it.valid[1] ? max(it.jhi[0], it.jhi[1]) : it.jhi[0]) : it.jhi[1];
+    it.n_kv = J1 - it.J0 + 1;
+    it.tok0 = tok0;
+    it.qlen = qlen;
+    it.batch = batch;
+    it.kvlen = kvlen;
+    it.qoff = qoff;
+    it.sq = sq;
+    it.g = it.head[0] / (p.Hq / p.Hkv);
+    return true;
+}
+
+// whether tile t takes part in key tile J0 + i of the item
+__device__ __forceinline__ bool prefill_uses(const PrefillItem &it, int t, int i) {
+    const int j = it.J0 + i;
+    return it.valid[t] && j >= it.jlo[t] && j <= it.jhi[t];
+}
 
 // PAGED: keys and values come from a cache of 16-token pages through the page
 // table (eight page boxes per 128-key tile, assembled into the same shared-memory
@@ -123,7 +254,7 @@ enum : uint32_t {
 // 2 = output with the statistics known (P = 2^(s * scale * log2e - LSE * log2e)
 // needs no running maximum and no rescaling; O = P V).
 template <int D, bool PAGED, int PASS = 0>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     using C = PrefillCfg<D>;
@@ -135,87 +266,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         (p.cu_seqlens[0] != 0 || p.cu_seqlens[p.nseq] != p.total))
         record_status(p.status, kStatusBounds);
 
-    // ---- work item: heaviest query tiles first, heads fastest (a key/value head's
-    //      query heads run together and share its K/V tiles in L2)
-    const int hunits = p.head_pairs ? p.Hq / 2 : p.Hq;
-    const int units = hunits * p.nseq;
-    const int nouter = p.head_pairs ? p.ntiles : (p.ntiles + 1) / 2;
-    const int outer = nouter - 1 - (int)(blockIdx.x / units);
-    const int rem = (int)(blockIdx.x % units);
-    const int hu = rem % hunits;
-    const int sq = rem / hunits;
-    // query rows [0, qlen) of this sequence sit at positions qoff + i; keys at [0, kvlen)
-    int tok0, qlen, batch;
-    if (p.cu_seqlens) {
-        tok0 = p.cu_seqlens[sq];
-        const int tend = p.cu_seqlens[sq + 1];
-        qlen = tend - tok0;
-        batch = 0;
-        // uniform: a sequence whose tokens leave [0, total) is skipped, nothing of it
-        // read or written; one longer than the launch's tiles has only those rows done
-        if (tok0 < 0 || tend < tok0 || tend > p.total) {
-            if (threadIdx.x == 0 && outer == nouter - 1 && hu == 0)
-                record_status(p.status, kStatusBounds);
-            return;
-        }
-        if (threadIdx.x == 0 && outer == nouter - 1 && hu == 0 &&
-            qlen > (p.tile0 + p.ntiles) * PrefillCfg<D>::BM)
-            record_status(p.status, kStatusBounds);
-    } else {
-        tok0 = 0;
-        qlen = p.N;
-        batch = sq;
-    }
-    int kvlen = qlen, qoff = 0;
-    if constexpr (PAGED) {
-        kvlen = p.kv_lens[sq];
-        qoff = kvlen - qlen;
-        if (qoff < 0 || kvlen > p.maxp * 16) {  // uniform: the sequence's sizes are invalid
-            if (threadIdx.x == 0 && outer == nouter - 1 && qlen > 0)
-                record_status(p.status, kStatusBounds);
-            return;
-        }
-    }
-    // the CTA's two tiles: query head, first row, and the key tiles [jlo, jhi] each needs
-    int head[2], row0[2], jlo[2], jhi[2];
-    if (p.head_pairs) {
-        head[0] = 2 * hu;
-        head[1] = 2 * hu + 1;
-        row0[0] = row0[1] = (p.tile0 + outer) * C::BM;
-    } else {
-        head[0] = head[1] = hu;
-        row0[0] = (p.tile0 + 2 * outer) * C::BM;
-        row0[1] = row0[0] + C::BM;
-    }
-    const int row_end = min(qlen, (p.tile0 + p.ntiles) * C::BM);  // rows this launch runs
-    const int g = head[0] / (p.Hq / p.Hkv);
-    bool valid[2];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        valid[t] = outer >= 0 && row0[t] < row_end;
-        const int last_row = min(row0[t] + C::BM, qlen) - 1;
-        const int lo_key = p.wl < 0 ? 0 : max(0, qoff + row0[t] - p.wl);
-        const int hi_key = p.wr < 0 ? kvlen - 1 : min(kvlen - 1, qoff + last_row + p.wr);
-        jlo[t] = lo_key / C::BN;
-        jhi[t] = hi_key / C::BN;
-    }
-    if (!valid[0] && !valid[1]) return;  // uniform: nothing to do
-    // key tiles J0 .. J0 + n_kv - 1 cover both tiles; ring slots count from J0
-    const int J0 = valid[0] ? (valid[1] ? min(jlo[0], jlo[1]) : jlo[0]) : jlo[1];
-    const int J1 = valid[0] ? (valid[1] ? max(jhi[0], jhi[1]) : jhi[0]) : jhi[1];
-    const int n_kv = J1 - J0 + 1;
-    // tile t takes part in key tile J0 + i
-    auto uses = [&](int t, int i) {
-        const int j = J0 + i;
-        return (t ? valid[1] : valid[0]) && j >= (t ? jlo[1] : jlo[0]) &&
-               j <= (t ? jhi[1] : jhi[0]);
-    };
+    const int n_items = prefill_items(p);
+    const int G = (int)gridDim.x;
 
     const uint32_t raw = smem_u32(pf_smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *base_ptr = pf_smem_raw + (base - raw);
     const uint32_t ctrl = base + C::OFF_CTRL;
     uint8_t *ctrl_ptr = base_ptr + C::OFF_CTRL;
+    float *stats = reinterpret_cast<float *>(base_ptr + C::OFF_STATS);  // [2][128]
     auto bar = [&](uint32_t i) { return ctrl + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(ctrl_ptr + 8 * BAR_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl_ptr + 8 * BAR_COUNT + 4);
@@ -223,8 +282,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 256) {
-        mbar_init(bar(BAR_Q), 1);
+    if (threadIdx.x == 384) {
+        mbar_init(bar(BAR_QFULL), 1);
+        mbar_init(bar(BAR_QEMPTY), 1);
         for (int s = 0; s < C::SK; ++s) {
             mbar_init(bar(BAR_KFULL + s), 1);
             mbar_init(bar(BAR_KEMPTY + s), 1);
@@ -237,12 +297,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             mbar_init(bar(BAR_SFULL + t), 1);
             mbar_init(bar(BAR_PFULL + t), 4);
             mbar_init(bar(BAR_OFULL + t), 1);
+            mbar_init(bar(BAR_OEMPTY + t), 4);
+            mbar_init(bar(BAR_STATS + t), 4);
+            mbar_init(bar(BAR_STATSE + t), 4);
         }
         mbar_init(bar(BAR_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tmem_alloc(ctrl + 8 * BAR_COUNT, 512);
         tmem_relinquish();
     }
@@ -251,7 +314,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
+    // (each role lowers or raises its warpgroup's registers first thing, so that the
+    // register limit of its code is the new count)
+    if (warp >= 12) {
+    setmaxnreg_dec<C::REG_OTHER>();
+    if (warp == 12) {
         // ============================ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmQ);
@@ -259,111 +326,148 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             prefetch_tmap(&tmV);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            mbar_arrive_expect_tx(bar(BAR_Q), (uint32_t)(valid[0] + valid[1]) * C::TILE);
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (!valid[t]) continue;
-#pragma unroll
-                for (int hf = 0; hf < C::NH; ++hf)
-                    tma_load_4d(base + C::OFF_Q + t * C::TILE + hf * C::HALF, &tmQ, bar(BAR_Q),
-                                hf * 64, head[t], tok0 + row0[t], batch, pol_q);
-            }
-            int issued_k = 0, issued_v = 0;
-            const int npg = (kvlen + 15) / 16;  // pages holding this sequence's keys
-            // PAGED: page ids of key tile J0 + j (eight 16-token pages), read one tile
-            // ahead so the loads overlap the waits; -1 past the sequence
-            int ids_next[8];
-            auto read_ids = [&](int j) {
-#pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) {
-                    const int pg = (J0 + j) * 8 + q8;
-                    ids_next[q8] = (j < n_kv && pg < npg)
-                                       ? p.page_table[(long long)sq * p.maxp + pg] : -1;
+            int kvc = 0;                     // key tiles loaded so far (ring position)
+            int nq = 0;                      // items whose query tiles were loaded
+            int issued_k = 0, issued_v = 0;  // ring positions issued
+            bool ok = true;
+            for (int r = 0; ok && r * G < n_items; ++r) {
+                const int idx = prefill_item_index(r);
+                PrefillItem it;
+                if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, true, it)) continue;
+                // both query tiles, once the previous item's QK products are done with theirs
+                if (!mbar_wait(bar(BAR_QEMPTY), ((uint32_t)nq & 1u) ^ 1u, p.status, abort_flag)) {
+                    ok = false;
+                    break;
                 }
-            };
-            if constexpr (PAGED) read_ids(0);
-            for (int j = 0; j < n_kv; ++j) {
-                const int kvrow = tok0 + (J0 + j) * C::BN;
-                // a page past the sequence, or a page id out of range (reported), is
-                // loaded from an out-of-range page coordinate: the copy fills zeros
-                int pcoord[8];
-                if constexpr (PAGED) {
+                mbar_arrive_expect_tx(bar(BAR_QFULL), (uint32_t)(it.valid[0] + it.valid[1]) * C::TILE);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!it.valid[t]) continue;
+#pragma unroll
+                    for (int hf = 0; hf < C::NH; ++hf)
+                        tma_load_4d(base + C::OFF_Q + t * C::TILE + hf * C::HALF, &tmQ,
+                                    bar(BAR_QFULL), hf * 64, it.head[t], it.tok0 + it.row0[t],
+                                    it.batch, pol_q);
+                }
+                ++nq;
+                // the next item's query tiles into L2 while this item runs
+                {
+                    const int idx2 = prefill_item_index(r + 1);
+                    PrefillItem nx;
+                    if (idx2 < n_items && prefill_item<D, PAGED>(p, idx2, false, nx)) {
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            if (!nx.valid[t]) continue;
+#pragma unroll
+                            for (int hf = 0; hf < C::NH; ++hf)
+                                tma_prefetch_4d(&tmQ, hf * 64, nx.head[t], nx.tok0 + nx.row0[t],
+                                                nx.batch);
+                        }
+                    }
+                }
+                const int npg = (it.kvlen + 15) / 16;  // pages holding this sequence's keys
+                // PAGED: page ids of key tile J0 + j (eight 16-token pages), read one tile
+                // ahead so the loads overlap the waits; -1 past the sequence
+                int ids_next[8];
+                auto read_ids = [&](int j) {
 #pragma unroll
                     for (int q8 = 0; q8 < 8; ++q8) {
-                        const int pg = (J0 + j) * 8 + q8;
-                        int pid = ids_next[q8];
-                        if (pg >= npg) {
-                            pid = p.num_pages;
-                        } else if ((unsigned)pid >= (unsigned)p.num_pages) {
-                            record_status(p.status, kStatusBounds);
-                            pid = p.num_pages;
+                        const int pg = (it.J0 + j) * 8 + q8;
+                        ids_next[q8] = (j < it.n_kv && pg < npg)
+                                           ? p.page_table[(long long)it.sq * p.maxp + pg] : -1;
+                    }
+                };
+                if constexpr (PAGED) read_ids(0);
+                for (int j = 0; j < it.n_kv; ++j) {
+                    const int kv = kvc + j;
+                    const int kvrow = it.tok0 + (it.J0 + j) * C::BN;
+                    // a page past the sequence, or a page id out of range (reported), is
+                    // loaded from an out-of-range page coordinate: the copy fills zeros
+                    int pcoord[8];
+                    if constexpr (PAGED) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 8; ++q8) {
+                            const int pg = (it.J0 + j) * 8 + q8;
+                            int pid = ids_next[q8];
+                            if (pg >= npg) {
+                                pid = p.num_pages;
+                            } else if ((unsigned)pid >= (unsigned)p.num_pages) {
+                                record_status(p.status, kStatusBounds);
+                                pid = p.num_pages;
+                            }
+                            pcoord[q8] = pid;
                         }
-                        pcoord[q8] = pid;
+                        read_ids(j + 1);
                     }
-                    read_ids(j + 1);
-                }
-                const int sk = j % C::SK;
-                if (!mbar_wait(bar(BAR_KEMPTY + sk), ((uint32_t)(j / C::SK) & 1u) ^ 1u, p.status,
-                               abort_flag))
-                    break;
-                mbar_arrive_expect_tx(bar(BAR_KFULL + sk), C::TILE);
-#pragma unroll
-                for (int hf = 0; hf < C::NH; ++hf) {
-                    const uint32_t dst = base + C::OFF_K + sk * C::TILE + hf * C::HALF;
-                    if constexpr (PAGED) {
-#pragma unroll
-                        for (int q8 = 0; q8 < 8; ++q8)
-                            tma_load_4d(dst + q8 * 2048u, &tmK, bar(BAR_KFULL + sk), hf * 64, 0,
-                                        g, pcoord[q8], pol_kv);
-                    } else {
-                        tma_load_4d(dst, &tmK, bar(BAR_KFULL + sk), hf * 64, g, kvrow, batch,
-                                    pol_kv);
+                    const int sk = kv % C::SK;
+                    if (!mbar_wait(bar(BAR_KEMPTY + sk), ((uint32_t)(kv / C::SK) & 1u) ^ 1u,
+                                   p.status, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                }
-                issued_k = j + 1;
-                if constexpr (PASS == 1) continue;  // the statistics need no values
-                const int sv = j % C::SV;
-                if (!mbar_wait(bar(BAR_VEMPTY + sv), ((uint32_t)(j / C::SV) & 1u) ^ 1u, p.status,
-                               abort_flag))
-                    break;
-                mbar_arrive_expect_tx(bar(BAR_VFULL + sv), C::TILE);
+                    mbar_arrive_expect_tx(bar(BAR_KFULL + sk), C::TILE);
 #pragma unroll
-                for (int hf = 0; hf < C::NH; ++hf) {
-                    const uint32_t dst = base + C::OFF_V + sv * C::TILE + hf * C::HALF;
-                    if constexpr (PAGED) {
+                    for (int hf = 0; hf < C::NH; ++hf) {
+                        const uint32_t dst = base + C::OFF_K + sk * C::TILE + hf * C::HALF;
+                        if constexpr (PAGED) {
 #pragma unroll
-                        for (int q8 = 0; q8 < 8; ++q8)
-                            tma_load_4d(dst + q8 * 2048u, &tmV, bar(BAR_VFULL + sv), hf * 64, 0,
-                                        g, pcoord[q8], pol_kv);
-                    } else {
-                        tma_load_4d(dst, &tmV, bar(BAR_VFULL + sv), hf * 64, g, kvrow, batch,
-                                    pol_kv);
+                            for (int q8 = 0; q8 < 8; ++q8)
+                                tma_load_4d(dst + q8 * 2048u, &tmK, bar(BAR_KFULL + sk), hf * 64,
+                                            0, it.g, pcoord[q8], pol_kv);
+                        } else {
+                            tma_load_4d(dst, &tmK, bar(BAR_KFULL + sk), hf * 64, it.g, kvrow,
+                                        it.batch, pol_kv);
+                        }
                     }
+                    issued_k = kv + 1;
+                    if constexpr (PASS == 1) continue;  // the statistics need no values
+                    const int sv = kv % C::SV;
+                    if (!mbar_wait(bar(BAR_VEMPTY + sv), ((uint32_t)(kv / C::SV) & 1u) ^ 1u,
+                                   p.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(BAR_VFULL + sv), C::TILE);
+#pragma unroll
+                    for (int hf = 0; hf < C::NH; ++hf) {
+                        const uint32_t dst = base + C::OFF_V + sv * C::TILE + hf * C::HALF;
+                        if constexpr (PAGED) {
+#pragma unroll
+                            for (int q8 = 0; q8 < 8; ++q8)
+                                tma_load_4d(dst + q8 * 2048u, &tmV, bar(BAR_VFULL + sv), hf * 64,
+                                            0, it.g, pcoord[q8], pol_kv);
+                        } else {
+                            tma_load_4d(dst, &tmV, bar(BAR_VFULL + sv), hf * 64, it.g, kvrow,
+                                        it.batch, pol_kv);
+                        }
+                    }
+                    issued_v = kv + 1;
                 }
-                issued_v = j + 1;
+                kvc += it.n_kv;
             }
             if (*abort_flag) {
                 // let the copies already issued land before the CTA exits
-                for (int j = max(0, issued_k - C::SK); j < issued_k; ++j)
-                    mbar_wait(bar(BAR_KFULL + j % C::SK), (uint32_t)(j / C::SK) & 1u, p.status,
+                for (int kv = max(0, issued_k - C::SK); kv < issued_k; ++kv)
+                    mbar_wait(bar(BAR_KFULL + kv % C::SK), (uint32_t)(kv / C::SK) & 1u, p.status,
                               nullptr);
-                for (int j = max(0, issued_v - C::SV); j < issued_v; ++j)
-                    mbar_wait(bar(BAR_VFULL + j % C::SV), (uint32_t)(j / C::SV) & 1u, p.status,
+                for (int kv = max(0, issued_v - C::SV); kv < issued_v; ++kv)
+                    mbar_wait(bar(BAR_VFULL + kv % C::SV), (uint32_t)(kv / C::SV) & 1u, p.status,
                               nullptr);
-                mbar_wait(bar(BAR_Q), 0u, p.status, nullptr);
+                if (nq > 0)
+                    mbar_wait(bar(BAR_QFULL), (uint32_t)(nq - 1) & 1u, p.status, nullptr);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ============================ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
             // PV: V is MN-major; its two 64-dim halves (128-byte swizzle atoms) lie 16 KB
             // apart, which the descriptor's leading offset describes
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-            // S_t = Q_t K_j^T into S buffer t
-            auto issue_qk = [&](int t, int j) {
+            // S_t = Q_t K^T (K in ring stage sk) into S buffer t
+            auto issue_qk = [&](int t, int sk) {
                 const uint32_t qb = base + C::OFF_Q + t * C::TILE;
-                const uint32_t kb = base + C::OFF_K + (j % C::SK) * C::TILE;
+                const uint32_t kb = base + C::OFF_K + sk * C::TILE;
                 const uint32_t dcol = tmem + (t ? C::COL_S1 : C::COL_S0);
                 // descriptors built once per product; each of the D/16 steps advances the
                 // start address by a constant (32 bytes within a 64-dim half, 16 KB between)
@@ -381,303 +485,398 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 }
                 tc_commit(bar(BAR_SFULL + t));
             };
-            bool ok = mbar_wait(bar(BAR_Q), 0u, p.status, abort_flag) &&
-                      mbar_wait(bar(BAR_KFULL + 0), 0u, p.status, abort_flag);
-            if (ok) {
+            int kvc = 0;                 // key tiles consumed so far (ring position)
+            int nq = 0;                  // items whose query tiles were used
+            int pc[2] = {0, 0};          // P hand-offs consumed per tile
+            int oc[2] = {0, 0};          // items per tile whose O was produced
+            bool ok = true;
+            for (int r = 0; ok && r * G < n_items; ++r) {
+                const int idx = prefill_item_index(r);
+                PrefillItem it;
+                if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, false, it)) continue;
+                const int kv0 = kvc;
+                ok = mbar_wait(bar(BAR_QFULL), (uint32_t)nq & 1u, p.status, abort_flag) &&
+                     mbar_wait(bar(BAR_KFULL + kv0 % C::SK), (uint32_t)(kv0 / C::SK) & 1u,
+                               p.status, abort_flag);
+                if (!ok) break;
+                ++nq;
                 tc_fence_after();
 #pragma unroll
                 for (int t = 0; t < 2; ++t)
-                    if (uses(t, 0)) issue_qk(t, 0);
-                tc_commit(bar(BAR_KEMPTY + 0));
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int sv = j % C::SV;
-                const int sk1 = (j + 1) % C::SK;
-                // the value tile of this step and the key tile of the next are waited for
-                // first: they are normally in place, and checking them while the softmax
-                // still works keeps those checks off the path from P to the next product
-                // (every key tile of [J0, J1] is used by at least one query tile)
-                const bool k_ready = j + 1 < n_kv;
-                if (PASS != 1 && !mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(j / C::SV) & 1u,
-                                            p.status, abort_flag))
-                    break;
-                if (k_ready && !mbar_wait(bar(BAR_KFULL + sk1), (uint32_t)((j + 1) / C::SK) & 1u,
-                                          p.status, abort_flag))
-                    break;
+                    if (prefill_uses(it, t, 0)) issue_qk(t, kv0 % C::SK);
+                if (it.n_kv == 1) tc_commit(bar(BAR_QEMPTY));  // the item's last QK product
+                tc_commit(bar(BAR_KEMPTY + kv0 % C::SK));
+                for (int j = 0; ok && j < it.n_kv; ++j) {
+                    const int kv = kvc + j;
+                    const int sv = kv % C::SV;
+                    const int sk1 = (kv + 1) % C::SK;
+                    // the value tile of this step and the key tile of the next are waited for
+                    // first: they are normally in place, and checking them while the softmax
+                    // still works keeps those checks off the path from P to the next product
+                    // (every key tile of the item is used by at least one query tile)
+                    const bool k_ready = j + 1 < it.n_kv;
+                    if (PASS != 1 && !mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(kv / C::SV) & 1u,
+                                                p.status, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (k_ready && !mbar_wait(bar(BAR_KFULL + sk1),
+                                              (uint32_t)((kv + 1) / C::SK) & 1u, p.status,
+                                              abort_flag)) {
+                        ok = false;
+                        break;
+                    }
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    // ring index j counts from J0; tile t's own count from its first key tile
-                    const int it = J0 + j - (t ? jlo[1] : jlo[0]);
-                    if (uses(t, j)) {
-                        // (statistics pass: PFULL says the S tile has been read)
-                        if (!mbar_wait(bar(BAR_PFULL + t), (uint32_t)it & 1u, p.status, abort_flag)) {
-                            ok = false;
-                            break;
+                    for (int t = 0; t < 2; ++t) {
+                        if (prefill_uses(it, t, j)) {
+                            // (statistics pass: PFULL says the S tile has been read)
+                            if (!mbar_wait(bar(BAR_PFULL + t), (uint32_t)pc[t] & 1u, p.status,
+                                           abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            ++pc[t];
+                            if constexpr (PASS != 1) {
+                                // the item's first product into O_t waits until the epilogue
+                                // has read the previous item's O_t
+                                const bool first = it.J0 + j == it.jlo[t];
+                                if (first && !mbar_wait(bar(BAR_OEMPTY + t),
+                                                        ((uint32_t)oc[t] & 1u) ^ 1u, p.status,
+                                                        abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                // O_t += P_t V_j: P_t (bf16, 128 x 128) from the S_t columns
+                                const uint32_t vb = base + C::OFF_V + sv * C::TILE;
+                                const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
+                                const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
+                                const SmemDesc vd = smem_desc_parts(vb, C::HALF, 1024);
+                                tc_mma_ts_off<0>(ocol, pcol, vd, idesc_pv, first ? 0u : 1u);
+                                tc_mma_ts_off<2048>(ocol, pcol + 8, vd, idesc_pv, 1u);
+                                tc_mma_ts_off<4096>(ocol, pcol + 16, vd, idesc_pv, 1u);
+                                tc_mma_ts_off<6144>(ocol, pcol + 24, vd, idesc_pv, 1u);
+                                tc_mma_ts_off<8192>(ocol, pcol + 32, vd, idesc_pv, 1u);
+                                tc_mma_ts_off<10240>(ocol, pcol + 40, vd, idesc_pv, 1u);
+                                tc_mma_ts_off<12288>(ocol, pcol + 48, vd, idesc_pv, 1u);
+                                tc_mma_ts_off<14336>(ocol, pcol + 56, vd, idesc_pv, 1u);
+                                if (!prefill_uses(it, t, j + 1)) tc_commit(bar(BAR_OFULL + t));
+                            }
+                        }
+                        if (prefill_uses(it, t, j + 1)) {
+                            tc_fence_after();
+                            issue_qk(t, sk1);
                         }
                     }
-                    if (PASS != 1 && uses(t, j)) {
-                        tc_fence_after();
-                        // O_t += P_t V_j: P_t (bf16, 128 x 128) from the S_t columns of TMEM
-                        const uint32_t vb = base + C::OFF_V + sv * C::TILE;
-                        const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
-                        const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
-                        const SmemDesc vd = smem_desc_parts(vb, C::HALF, 1024);
-                        tc_mma_ts_off<0>(ocol, pcol, vd, idesc_pv, it > 0 ? 1u : 0u);
-                        tc_mma_ts_off<2048>(ocol, pcol + 8, vd, idesc_pv, 1u);
-                        tc_mma_ts_off<4096>(ocol, pcol + 16, vd, idesc_pv, 1u);
-                        tc_mma_ts_off<6144>(ocol, pcol + 24, vd, idesc_pv, 1u);
-                        tc_mma_ts_off<8192>(ocol, pcol + 32, vd, idesc_pv, 1u);
-                        tc_mma_ts_off<10240>(ocol, pcol + 40, vd, idesc_pv, 1u);
-                        tc_mma_ts_off<12288>(ocol, pcol + 48, vd, idesc_pv, 1u);
-                        tc_mma_ts_off<14336>(ocol, pcol + 56, vd, idesc_pv, 1u);
-                        if (!uses(t, j + 1)) tc_commit(bar(BAR_OFULL + t));
-                    }
-                    if (uses(t, j + 1)) {
-                        tc_fence_after();
-                        issue_qk(t, j + 1);
-                    }
+                    if (!ok) break;
+                    if (j + 2 == it.n_kv) tc_commit(bar(BAR_QEMPTY));  // the item's last QK
+                    if (PASS != 1) tc_commit(bar(BAR_VEMPTY + sv));
+                    if (k_ready) tc_commit(bar(BAR_KEMPTY + sk1));
                 }
                 if (!ok) break;
-                if (PASS != 1) tc_commit(bar(BAR_VEMPTY + sv));
-                if (k_ready) tc_commit(bar(BAR_KEMPTY + sk1));
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                    if (it.valid[t]) ++oc[t];
+                kvc += it.n_kv;
             }
             // all issued MMAs complete before TMEM is released
             tc_commit(bar(BAR_DRAIN));
             mbar_wait(bar(BAR_DRAIN), 0u, p.status, nullptr);
         }
+    }
     } else if (warp < 8) {
         // ============================ softmax: warpgroup t, thread = query row
+        setmaxnreg_inc<C::REG_SOFTMAX>();
         const int t = warp >> 2;
-        const int j_first = t ? jlo[1] : jlo[0];
-        const int n_mine = (t ? valid[1] : valid[0]) ? (t ? jhi[1] : jhi[0]) - j_first + 1 : 0;
         const int r = threadIdx.x & 127;           // row in tile = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t scol = tmem + lane_base + (t ? C::COL_S1 : C::COL_S0);
         const uint32_t ocol = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
-        const int qpos = (t ? row0[1] : row0[0]) + r;  // position within the sequence
-        // allowed keys of this row: [klo, khi]
-        const int klo = p.wl < 0 ? 0 : qoff + qpos - p.wl;
-        const int khi = p.wr < 0 ? kvlen - 1 : min(kvlen - 1, qoff + qpos + p.wr);
-        float m_ref = -INFINITY;                   // log2 units, scaled
-        float l = 0.f;                             // sum of P (fp32) -> LSE
-        float lr = 0.f;                            // sum of bf16-rounded P -> normalises O
         const float sl2 = p.scale_log2;
-        const long long lse_idx = p.cu_seqlens ? (long long)(t ? head[1] : head[0]) * p.total +
-                                                     tok0 + qpos
-                                               : ((long long)batch * p.Hq +
-                                                  (t ? head[1] : head[0])) * p.N + qpos;
-        if constexpr (PASS == 2) {
-            // the row's statistics from the first pass: P = 2^(s * sl2 - LSE * log2e)
-            const float lse_row = qpos < qlen ? p.lse[lse_idx] : 0.f;
-            m_ref = lse_row * kLog2e;
-        }
+        int sc = 0;   // S tiles consumed (SFULL phases)
+        int oc = 0;   // items of this tile (STATS / STATSE phases)
         bool ok = true;
-        for (int j = 0; j < n_mine; ++j) {
-            ok = mbar_wait(bar(BAR_SFULL + t), (uint32_t)j & 1u, p.status, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
+        for (int rr = 0; ok && rr * G < n_items; ++rr) {
+            const int idx = prefill_item_index(rr);
+            PrefillItem it;
+            if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, false, it)) continue;
+            if (!it.valid[t]) continue;
+            const int j_first = it.jlo[t];
+            const int n_mine = it.jhi[t] - j_first + 1;
+            const int qpos = it.row0[t] + r;  // position within the sequence
+            // allowed keys of this row: [klo, khi]
+            const int klo = p.wl < 0 ? 0 : it.qoff + qpos - p.wl;
+            const int khi = p.wr < 0 ? it.kvlen - 1 : min(it.kvlen - 1, it.qoff + qpos + p.wr);
+            float m_ref = -INFINITY;                   // log2 units, scaled
+            float l = 0.f;                             // sum of P (fp32) -> LSE
+            float lr = 0.f;                            // sum of bf16-rounded P -> normalises O
+            const long long lse_idx = p.cu_seqlens
+                                          ? (long long)it.head[t] * p.total + it.tok0 + qpos
+                                          : ((long long)it.batch * p.Hq + it.head[t]) * p.N + qpos;
+            if constexpr (PASS == 2) {
+                // the row's statistics from the first pass: P = 2^(s * sl2 - LSE * log2e)
+                const float lse_row = qpos < it.qlen ? p.lse[lse_idx] : 0.f;
+                m_ref = lse_row * kLog2e;
             }
-            tc_fence_after();
-            uint32_t sr[128];
-            float *s = reinterpret_cast<float *>(sr);
-            const int kv0 = (j_first + j) * C::BN;
-            // the S row from TMEM, keys outside [klo, khi] masked
-            auto load_s = [&]() {
-                tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-                tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-                tc_wait_ld();
-                if (kv0 < klo || kv0 + C::BN - 1 > khi) {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (kv0 + c < klo || kv0 + c > khi) s[c] = -INFINITY;
+            for (int j = 0; j < n_mine; ++j) {
+                ok = mbar_wait(bar(BAR_SFULL + t), (uint32_t)sc & 1u, p.status, abort_flag);
+                ++sc;
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
                 }
-            };
-            load_s();
-            if constexpr (PASS == 1) {
-                // the S tile is in registers: the next one may overwrite it
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
-            }
-            bool p_done = false;
-            if constexpr (PASS == 1) {
-                // Statistics pass, fast path: while the reference stands only the sum of P
-                // is needed (same bound as below).  The S row stays in registers (no P is
-                // stored), so a tile whose sum passes 2^24 goes on to the maximum below.
-                if (__all_sync(0xffffffffu, j > 0 && m_ref != -INFINITY)) {
-                    float fe[4] = {0.f, 0.f, 0.f, 0.f};
+                tc_fence_after();
+                uint32_t sr[128];
+                float *s = reinterpret_cast<float *>(sr);
+                const int kv0 = (j_first + j) * C::BN;
+                const bool masked = kv0 < klo || kv0 + C::BN - 1 > khi;
+                // keys outside [klo, khi] of columns [c0, c0 + 64) masked
+                auto mask_half = [&](int c0) {
+                    if (masked) {
 #pragma unroll
-                    for (int c = 0; c < 128; c += 2) {
-                        float t0, t1;
-                        ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_ref, -m_ref);
-                        const int a = (c >> 1) & 1;
-                        fadd2(fe[2 * a], fe[2 * a + 1], ex2(t0), ex2(t1));
+                        for (int c = c0; c < c0 + 64; ++c)
+                            if (kv0 + c < klo || kv0 + c > khi) s[c] = -INFINITY;
                     }
-                    const float lt = (fe[0] + fe[1]) + (fe[2] + fe[3]);
-                    if (__all_sync(0xffffffffu, lt <= 16777216.f)) {
-                        l += lt;
-                        p_done = true;
+                };
+                // the S row from TMEM, masked
+                auto load_s = [&]() {
+                    tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                    tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+                    tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+                    tc_wait_ld();
+                    mask_half(0);
+                    mask_half(64);
+                };
+                // one-pass fast path (below): after a row's first key tile
+                const bool fast = PASS == 0 && __all_sync(0xffffffffu, j > 0 && m_ref != -INFINITY);
+                if (!fast) load_s();
+                if constexpr (PASS == 1) {
+                    // the S tile is in registers: the next one may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
+                }
+                bool p_done = false;
+                if constexpr (PASS == 1) {
+                    // Statistics pass, fast path: while the reference stands only the sum of P
+                    // is needed (same bound as below).  The S row stays in registers (no P is
+                    // stored), so a tile whose sum passes 2^24 goes on to the maximum below.
+                    if (__all_sync(0xffffffffu, j > 0 && m_ref != -INFINITY)) {
+                        float fe[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int c = 0; c < 128; c += 2) {
+                            float t0, t1;
+                            ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_ref, -m_ref);
+                            const int a = (c >> 1) & 1;
+                            fadd2(fe[2 * a], fe[2 * a + 1], ex2(t0), ex2(t1));
+                        }
+                        const float lt = (fe[0] + fe[1]) + (fe[2] + fe[3]);
+                        if (__all_sync(0xffffffffu, lt <= 16777216.f)) {
+                            l += lt;
+                            p_done = true;
+                        }
                     }
                 }
-            }
-            if constexpr (PASS == 0) {
-                // Fast path: try P against the current reference maximum first.  If no
-                // row's sum of P over this tile exceeds 2^24, no element exceeds the
-                // reference by more than 24 (log2 units): P, the sums and O stay far
-                // inside the fp32/bf16 range (relative precision does not depend on the
-                // scale), so the reference stands and the row maximum is never needed.
-                // Otherwise reload the S tile (it is still in TMEM) and take the path
-                // with the maximum below, which moves the reference when it is exceeded
-                // by more than 8.
-                if (__all_sync(0xffffffffu, j > 0 && m_ref != -INFINITY)) {
-                    float fe[4] = {0.f, 0.f, 0.f, 0.f};
-                    float fq[2] = {0.f, 0.f};
-                    uint32_t pk[64];
+                if constexpr (PASS == 0) {
+                    // Fast path: try P against the current reference maximum first.  If no
+                    // row's sum of P over this tile exceeds 2^24, no element exceeds the
+                    // reference by more than 24 (log2 units): P, the sums and O stay far
+                    // inside the fp32/bf16 range (relative precision does not depend on the
+                    // scale), so the reference stands and the row maximum is never needed.
+                    // The S row arrives in two halves: the second half's load is in flight
+                    // while the first half's P is computed and stored, and each 32 keys' P
+                    // goes to TMEM as soon as it is packed (over S columns already read).
+                    // Otherwise the S row is still in registers: the path with the maximum
+                    // below recomputes P over the same columns, moving the reference when
+                    // it is exceeded by more than 8.
+                    if (fast) {
+                        tmem_ld32(scol + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                        tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                        tc_wait_ld();
+                        tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+                        tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+                        mask_half(0);
+                        float fe[4] = {0.f, 0.f, 0.f, 0.f};
+                        float fq[2] = {0.f, 0.f};
 #pragma unroll
-                    for (int c = 0; c < 128; c += 2) {
+                        for (int cb = 0; cb < 128; cb += 32) {
+                            if (cb == 64) {
+                                tc_wait_ld();
+                                mask_half(64);
+                            }
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int c = cb; c < cb + 32; c += 2) {
+                                float t0, t1;
+                                ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_ref, -m_ref);
+                                const float p0 = ex2(t0);
+                                const float p1 = ex2(t1);
+                                const int a = (c >> 1) & 1;
+                                fadd2(fe[2 * a], fe[2 * a + 1], p0, p1);
+                                const uint32_t pp = pack_bf16(p0, p1);
+                                add_bf16x2_to(fq[a], pp);
+                                pk[(c - cb) >> 1] = pp;
+                            }
+                            tmem_st16(scol + (cb >> 1), pk);
+                        }
+                        const float lt = (fe[0] + fe[1]) + (fe[2] + fe[3]);
+                        if (__all_sync(0xffffffffu, lt <= 16777216.f)) {
+                            l += lt;
+                            lr += fq[0] + fq[1];
+                            p_done = true;
+                        }
+                    }
+                }
+                // row maximum: eight independent 3-input max chains (the output pass of the
+                // two-pass form knows the row's statistics and skips this)
+                if (!p_done) {
+                if constexpr (PASS != 2) {
+                float mxa[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxa[i] = fmax3(s[i], s[i + 8], s[i + 16]);
+#pragma unroll
+                for (int c = 24; c + 16 <= 120; c += 16)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(mxa[i], s[120 + i]);
+                const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]),
+                                       fmax3(mxa[3], mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7]));
+                const float m_new = fmaxf(m_ref, mx * sl2);
+                const bool need = m_new > m_ref + 8.0f;
+                if (j == 0) {
+                    m_ref = m_new;
+                } else if (__any_sync(0xffffffffu, need)) {
+                    // O_t holds P_{j-1} V_{j-1} complete: the commit that signalled S_j
+                    // covers every MMA issued before it
+                    const float alpha = need ? ex2(m_ref - m_new) : 1.0f;
+                    if (need) {
+                        l *= alpha;
+                        lr *= alpha;
+                        m_ref = m_new;
+                    }
+#pragma unroll 1
+                    for (int c = 0; c < (PASS == 1 ? 0 : D); c += 16) {
+                        uint32_t orr[16];
+                        tmem_ld16(ocol + c, orr);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                        tmem_st16(ocol + c, orr);
+                    }
+                }
+                }  // PASS != 2
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                // P = 2^(s*scale*log2e - M); the exact row sum feeds the log-sum-exp, and the
+                // row sum of the bf16-rounded P (the values the PV product uses) normalises O,
+                // so O / L stays an exact convex combination of V rows.  P goes over the first
+                // 64 columns of the S buffer it came from, 32 values (16 columns) at a time,
+                // so the S registers of a chunk are free once it is stored.
+                float le[4] = {0.f, 0.f, 0.f, 0.f};
+                float lq[2] = {0.f, 0.f};
+#pragma unroll
+                for (int cb = 0; cb < 128; cb += 32) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = cb; c < cb + 32; c += 2) {
                         float t0, t1;
-                        ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_ref, -m_ref);
+                        ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_use, -m_use);
                         const float p0 = ex2(t0);
                         const float p1 = ex2(t1);
                         const int a = (c >> 1) & 1;
-                        fadd2(fe[2 * a], fe[2 * a + 1], p0, p1);
-                        const uint32_t pp = pack_bf16(p0, p1);
-                        add_bf16x2_to(fq[a], pp);
-                        pk[c >> 1] = pp;
+                        fadd2(le[2 * a], le[2 * a + 1], p0, p1);
+                        if constexpr (PASS != 1) {
+                            const uint32_t pp = pack_bf16(p0, p1);
+                            add_bf16x2_to(lq[a], pp);
+                            pk[(c - cb) >> 1] = pp;
+                        }
                     }
-                    const float lt = (fe[0] + fe[1]) + (fe[2] + fe[3]);
-                    if (__all_sync(0xffffffffu, lt <= 16777216.f)) {
-                        l += lt;
-                        lr += fq[0] + fq[1];
-                        tmem_st16(scol + 0, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-                        tmem_st16(scol + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
-                        tmem_st16(scol + 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[32]));
-                        tmem_st16(scol + 48, *reinterpret_cast<uint32_t(*)[16]>(&pk[48]));
-                        p_done = true;
-                    } else {
-                        load_s();
-                    }
+                    if constexpr (PASS != 1) tmem_st16(scol + (cb >> 1), pk);
+                }
+                l += (le[0] + le[1]) + (le[2] + le[3]);
+                lr += lq[0] + lq[1];
+                }  // !p_done
+                if constexpr (PASS != 1) {
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
                 }
             }
-            // row maximum: eight independent 3-input max chains (the output pass of the
-            // two-pass form knows the row's statistics and skips this)
-            if (!p_done) {
-            if constexpr (PASS != 2) {
-            float mxa[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mxa[i] = fmax3(s[i], s[i + 8], s[i + 16]);
-#pragma unroll
-            for (int c = 24; c + 16 <= 120; c += 16)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = fmax3(mxa[i], s[c + i], s[c + 8 + i]);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mxa[i] = fmaxf(mxa[i], s[120 + i]);
-            const float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
-                                   fmaxf(mxa[6], mxa[7]));
-            const float m_new = fmaxf(m_ref, mx * sl2);
-            const bool need = m_new > m_ref + 8.0f;
-            if (j == 0) {
-                m_ref = m_new;
-            } else if (__any_sync(0xffffffffu, need)) {
-                // O_t holds P_{j-1} V_{j-1} complete: the commit that signalled S_j
-                // covers every MMA issued before it
-                const float alpha = need ? ex2(m_ref - m_new) : 1.0f;
-                if (need) {
-                    l *= alpha;
-                    lr *= alpha;
-                    m_ref = m_new;
-                }
-#pragma unroll 1
-                for (int c = 0; c < (PASS == 1 ? 0 : D); c += 16) {
-                    uint32_t orr[16];
-                    tmem_ld16(ocol + c, orr);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                    tmem_st16(ocol + c, orr);
-                }
-            }
-            }  // PASS != 2
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            // P = 2^(s*scale*log2e - M); the exact row sum feeds the log-sum-exp, and the
-            // row sum of the bf16-rounded P (the values the PV product uses) normalises O,
-            // so O / L stays an exact convex combination of V rows.  P goes over the first
-            // 64 columns of the S buffer it came from, 32 values (16 columns) at a time,
-            // so the S registers of a chunk are free once it is stored.
-            float le[4] = {0.f, 0.f, 0.f, 0.f};
-            float lq[2] = {0.f, 0.f};
-#pragma unroll
-            for (int cb = 0; cb < 128; cb += 32) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = cb; c < cb + 32; c += 2) {
-                    float t0, t1;
-                    ffma2(t0, t1, s[c], s[c + 1], sl2, sl2, -m_use, -m_use);
-                    const float p0 = ex2(t0);
-                    const float p1 = ex2(t1);
-                    const int a = (c >> 1) & 1;
-                    fadd2(le[2 * a], le[2 * a + 1], p0, p1);
-                    if constexpr (PASS != 1) {
-                        const uint32_t pp = pack_bf16(p0, p1);
-                        add_bf16x2_to(lq[a], pp);
-                        pk[(c - cb) >> 1] = pp;
-                    }
-                }
-                if constexpr (PASS != 1) tmem_st16(scol + (cb >> 1), pk);
-            }
-            l += (le[0] + le[1]) + (le[2] + le[3]);
-            lr += lq[0] + lq[1];
-            }  // !p_done
+            if (!ok) break;
+            // ---- end of the item: LSE (the output pass takes it as input), and 1 / L
+            //      for the epilogue once it has read the previous item's
+            if (PASS != 2 && qpos < it.qlen && p.lse)
+                p.lse[lse_idx] = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
             if constexpr (PASS != 1) {
-                tc_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_PFULL + t));
-            }
-        }
-        if (ok && n_mine > 0) {
-            // ---- epilogue: O / L -> bf16, LSE (statistics pass: LSE only; output pass:
-            // O only, the LSE is its input)
-            if constexpr (PASS == 1) {
-                if (qpos < qlen && p.lse)
-                    p.lse[lse_idx] = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-                ok = false;
-            } else {
-                ok = mbar_wait(bar(BAR_OFULL + t), 0u, p.status, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-            }
-            if (ok) {
-                tc_fence_after();
-                const bool row_ok = qpos < qlen;
-                const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
-                const int h = t ? head[1] : head[0];
-                const long long tok = (long long)tok0 + qpos;
-                __nv_bfloat16 *orow =
-                    p.o + ((p.cu_seqlens ? tok : (long long)batch * p.N + qpos) * p.Hq + h) * D;
-#pragma unroll
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t orr[32];
-                    tmem_ld32(ocol + c, orr);
-                    tc_wait_ld();
-                    uint32_t pkd[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pkd[e] = pack_bf16(__uint_as_float(orr[2 * e]) * inv,
-                                           __uint_as_float(orr[2 * e + 1]) * inv);
-                    if (row_ok) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_uint4(pkd[4 * e], pkd[4 * e + 1], pkd[4 * e + 2],
-                                                pkd[4 * e + 3]);
-                    }
+                ok = mbar_wait(bar(BAR_STATSE + t), ((uint32_t)oc & 1u) ^ 1u, p.status, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
                 }
-                if (PASS == 0 && row_ok && p.lse)
-                    p.lse[lse_idx] = (l > 0.f) ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+                stats[t * 128 + r] = (lr > 0.f) ? 1.f / lr : 0.f;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_STATS + t));
+            }
+            ++oc;
+        }
+    } else {
+        // ============================ epilogue: thread = query row of both tiles
+        setmaxnreg_dec<C::REG_OTHER>();
+        if constexpr (PASS != 1) {
+            const int r = threadIdx.x & 127;       // row in tile = TMEM lane
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            int oc[2] = {0, 0};
+            bool ok = true;
+            for (int rr = 0; ok && rr * G < n_items; ++rr) {
+                const int idx = prefill_item_index(rr);
+                PrefillItem it;
+                if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, false, it)) continue;
+#pragma unroll 1
+                for (int t = 0; t < 2; ++t) {
+                    if (!it.valid[t]) continue;
+                    ok = mbar_wait(bar(BAR_STATS + t), (uint32_t)oc[t] & 1u, p.status, abort_flag);
+                    const float inv = stats[t * 128 + r];
+                    __syncwarp();
+                    if (lane == 0 && ok) mbar_arrive(bar(BAR_STATSE + t));
+                    ok = ok && mbar_wait(bar(BAR_OFULL + t), (uint32_t)oc[t] & 1u, p.status,
+                                         abort_flag);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ocol = tmem + lane_base + (t ? C::COL_O1 : C::COL_O0);
+                    const int qpos = it.row0[t] + r;
+                    const bool row_ok = qpos < it.qlen;
+                    const long long tok = (long long)it.tok0 + qpos;
+                    __nv_bfloat16 *orow =
+                        p.o + ((p.cu_seqlens ? tok : (long long)it.batch * p.N + qpos) * p.Hq +
+                               it.head[t]) * D;
+#pragma unroll
+                    for (int c = 0; c < D; c += 16) {
+                        uint32_t orr[16];
+                        tmem_ld16(ocol + c, orr);
+                        tc_wait_ld();
+                        uint32_t pkd[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pkd[e] = pack_bf16(__uint_as_float(orr[2 * e]) * inv,
+                                               __uint_as_float(orr[2 * e + 1]) * inv);
+                        if (row_ok) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+                            dst[0] = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+                            dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+                        }
+                    }
+                    // O_t is out of TMEM: the next item's first product may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(BAR_OEMPTY + t));
+                    ++oc[t];
+                }
             }
         }
     }
@@ -685,7 +884,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }

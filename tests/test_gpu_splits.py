@@ -76,7 +76,8 @@ def test_split_counts_match_the_oracle_and_repeat_bitwise(hook, oracle):
     o1, l1 = outs[1]
     for ctas, (o, l) in outs.items():
         assert float((o.float() - o1.float()).abs().max()) <= 2e-2, ctas
-        assert float((l - l1).abs().max()) <= 1e-3, ctas
+        empty = torch.isneginf(l) & torch.isneginf(l1)      # the 0-token sequence
+        assert float(torch.where(empty, 0.0, l - l1).abs().max()) <= 1e-3, ctas
     # the library's own launch is one of these counts (one CTA per SM for a bf16 cache)
     od, ld = A.attn_decode_paged(*dev, w.scale)
     torch.cuda.synchronize()
