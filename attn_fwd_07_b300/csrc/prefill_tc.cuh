@@ -41,8 +41,8 @@
 //                S_{j+1} never overwrites P_j before O += P_j V_j has read it,
 //                and a commit after S_{j+1} also covers that PV product.
 //   warps 14-15  idle (they complete the fourth warpgroup)
-// The softmax warpgroups raise their register count to 192 per thread; the
-// other two lower theirs to 64 (192 + 64 = twice the 128 of the launch).
+// The softmax warpgroups raise their register count to 184 per thread; the
+// other two lower theirs to 72 (184 + 72 = twice the 128 of the launch).
 //
 // Softmax step for tile t and key tile j (thread = row): load the S row from
 // TMEM, mask (causal diagonal / window / sequence end), running maximum, P =
@@ -114,7 +114,7 @@ struct PrefillCfg {
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
     static constexpr int THREADS = 512;
     // per-thread registers after the split: softmax warpgroups / the other two
-    static constexpr uint32_t REG_SOFTMAX = 192, REG_OTHER = 64;
+    static constexpr uint32_t REG_SOFTMAX = 184, REG_OTHER = 72;
 };
 
 static_assert(PrefillCfg<128>::SMEM <= 227 * 1024, "prefill shared memory");
@@ -464,15 +464,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             // PV: V is MN-major; its two 64-dim halves (128-byte swizzle atoms) lie 16 KB
             // apart, which the descriptor's leading offset describes
             constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 0, 1);
-            // S_t = Q_t K^T (K in ring stage sk) into S buffer t
-            auto issue_qk = [&](int t, int sk) {
-                const uint32_t qb = base + C::OFF_Q + t * C::TILE;
-                const uint32_t kb = base + C::OFF_K + sk * C::TILE;
+            // descriptors of the two query tiles (fixed) and of ring stage 0's K and V; a
+            // stage's descriptors are stage 0's advanced by the stage offset
+            const SmemDesc qd0 = smem_desc_parts(base + C::OFF_Q, 1024, 1024);
+            const SmemDesc qd1 = smem_desc_parts(base + C::OFF_Q + C::TILE, 1024, 1024);
+            const SmemDesc kd0 = smem_desc_parts(base + C::OFF_K, 1024, 1024);
+            const SmemDesc vd0 = smem_desc_parts(base + C::OFF_V, C::HALF, 1024);
+            // S_t = Q_t K^T (K in ring stage st) into S buffer t
+            auto issue_qk = [&](int t, int st) {
+                const SmemDesc qd = t ? qd1 : qd0;
+                const SmemDesc kd{kd0.lo + (uint32_t)st * (C::TILE >> 4), kd0.hi};
                 const uint32_t dcol = tmem + (t ? C::COL_S1 : C::COL_S0);
-                // descriptors built once per product; each of the D/16 steps advances the
-                // start address by a constant (32 bytes within a 64-dim half, 16 KB between)
-                const SmemDesc qd = smem_desc_parts(qb, 1024, 1024);
-                const SmemDesc kd = smem_desc_parts(kb, 1024, 1024);
+                // each of the D/16 steps advances the start addresses by a constant (32
+                // bytes within a 64-dim half, 16 KB between the halves)
                 tc_mma_ss_off<0, 0>(dcol, qd, kd, idesc_qk, 0u);
                 tc_mma_ss_off<32, 32>(dcol, qd, kd, idesc_qk, 1u);
                 tc_mma_ss_off<64, 64>(dcol, qd, kd, idesc_qk, 1u);
@@ -485,99 +489,120 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 }
                 tc_commit(bar(BAR_SFULL + t));
             };
-            int kvc = 0;                 // key tiles consumed so far (ring position)
+            // O_t += P_t V (V in ring stage st): P_t (bf16, 128 x 128) from the S_t columns
+            auto issue_pv = [&](int t, int st, uint32_t acc) {
+                const SmemDesc vd{vd0.lo + (uint32_t)st * (C::TILE >> 4), vd0.hi};
+                const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
+                const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
+                tc_mma_ts_off<0>(ocol, pcol, vd, idesc_pv, acc);
+                tc_mma_ts_off<2048>(ocol, pcol + 8, vd, idesc_pv, 1u);
+                tc_mma_ts_off<4096>(ocol, pcol + 16, vd, idesc_pv, 1u);
+                tc_mma_ts_off<6144>(ocol, pcol + 24, vd, idesc_pv, 1u);
+                tc_mma_ts_off<8192>(ocol, pcol + 32, vd, idesc_pv, 1u);
+                tc_mma_ts_off<10240>(ocol, pcol + 40, vd, idesc_pv, 1u);
+                tc_mma_ts_off<12288>(ocol, pcol + 48, vd, idesc_pv, 1u);
+                tc_mma_ts_off<14336>(ocol, pcol + 56, vd, idesc_pv, 1u);
+            };
+            // ring positions are kept as (stage, phase parity) and advanced one at a time:
+            // no division on the issuing thread's path
+            int ks = 0, vs = 0;          // K / V stages of the current key tile
+            uint32_t kph = 0, vph = 0;   // ... and the parities of their phases
             int nq = 0;                  // items whose query tiles were used
-            int pc[2] = {0, 0};          // P hand-offs consumed per tile
-            int oc[2] = {0, 0};          // items per tile whose O was produced
+            int pc0 = 0, pc1 = 0;        // P hand-offs consumed per tile
+            int oc0 = 0, oc1 = 0;        // items per tile whose O was produced
             bool ok = true;
             for (int r = 0; ok && r * G < n_items; ++r) {
                 const int idx = prefill_item_index(r);
                 PrefillItem it;
                 if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, false, it)) continue;
-                const int kv0 = kvc;
+                // steps [f_t, l_t] of the item use tile t (none for an invalid tile)
+                const int f0 = it.valid[0] ? it.jlo[0] - it.J0 : 1 << 30;
+                const int l0 = it.valid[0] ? it.jhi[0] - it.J0 : -1;
+                const int f1 = it.valid[1] ? it.jlo[1] - it.J0 : 1 << 30;
+                const int l1 = it.valid[1] ? it.jhi[1] - it.J0 : -1;
+                const int n_kv = it.n_kv;
                 ok = mbar_wait(bar(BAR_QFULL), (uint32_t)nq & 1u, p.status, abort_flag) &&
-                     mbar_wait(bar(BAR_KFULL + kv0 % C::SK), (uint32_t)(kv0 / C::SK) & 1u,
-                               p.status, abort_flag);
+                     mbar_wait(bar(BAR_KFULL + ks), kph, p.status, abort_flag);
                 if (!ok) break;
                 ++nq;
                 tc_fence_after();
-#pragma unroll
-                for (int t = 0; t < 2; ++t)
-                    if (prefill_uses(it, t, 0)) issue_qk(t, kv0 % C::SK);
-                if (it.n_kv == 1) tc_commit(bar(BAR_QEMPTY));  // the item's last QK product
-                tc_commit(bar(BAR_KEMPTY + kv0 % C::SK));
-                for (int j = 0; ok && j < it.n_kv; ++j) {
-                    const int kv = kvc + j;
-                    const int sv = kv % C::SV;
-                    const int sk1 = (kv + 1) % C::SK;
+                if (f0 == 0) issue_qk(0, ks);
+                if (f1 == 0) issue_qk(1, ks);
+                if (n_kv == 1) tc_commit(bar(BAR_QEMPTY));  // the item's last QK product
+                tc_commit(bar(BAR_KEMPTY + ks));
+                for (int j = 0; j < n_kv; ++j) {
+                    const int ks1 = ks + 1 == C::SK ? 0 : ks + 1;
+                    const uint32_t kph1 = ks1 == 0 ? kph ^ 1u : kph;
+                    const bool more = j + 1 < n_kv;
                     // the value tile of this step and the key tile of the next are waited for
                     // first: they are normally in place, and checking them while the softmax
-                    // still works keeps those checks off the path from P to the next product
+                    // still works keeps the checks off the path from P to the next product
                     // (every key tile of the item is used by at least one query tile)
-                    const bool k_ready = j + 1 < it.n_kv;
-                    if (PASS != 1 && !mbar_wait(bar(BAR_VFULL + sv), (uint32_t)(kv / C::SV) & 1u,
-                                                p.status, abort_flag)) {
+                    if (PASS != 1 && !mbar_wait(bar(BAR_VFULL + vs), vph, p.status, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    if (k_ready && !mbar_wait(bar(BAR_KFULL + sk1),
-                                              (uint32_t)((kv + 1) / C::SK) & 1u, p.status,
-                                              abort_flag)) {
+                    if (more && !mbar_wait(bar(BAR_KFULL + ks1), kph1, p.status, abort_flag)) {
                         ok = false;
                         break;
                     }
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (prefill_uses(it, t, j)) {
-                            // (statistics pass: PFULL says the S tile has been read)
-                            if (!mbar_wait(bar(BAR_PFULL + t), (uint32_t)pc[t] & 1u, p.status,
-                                           abort_flag)) {
+                    // tile 0, then tile 1: O_t += P_t V_j, S_t = Q_t K_{j+1}^T
+                    if (j >= f0 && j <= l0) {
+                        // (statistics pass: PFULL says the S tile has been read)
+                        if (!mbar_wait(bar(BAR_PFULL + 0), (uint32_t)pc0 & 1u, p.status,
+                                       abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        ++pc0;
+                        if constexpr (PASS != 1) {
+                            // the item's first product into O_0 waits until the epilogue has
+                            // read the previous item's O_0
+                            if (j == f0 && !mbar_wait(bar(BAR_OEMPTY + 0),
+                                                      ((uint32_t)oc0 & 1u) ^ 1u, p.status,
+                                                      abort_flag)) {
                                 ok = false;
                                 break;
                             }
-                            ++pc[t];
-                            if constexpr (PASS != 1) {
-                                // the item's first product into O_t waits until the epilogue
-                                // has read the previous item's O_t
-                                const bool first = it.J0 + j == it.jlo[t];
-                                if (first && !mbar_wait(bar(BAR_OEMPTY + t),
-                                                        ((uint32_t)oc[t] & 1u) ^ 1u, p.status,
-                                                        abort_flag)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after();
-                                // O_t += P_t V_j: P_t (bf16, 128 x 128) from the S_t columns
-                                const uint32_t vb = base + C::OFF_V + sv * C::TILE;
-                                const uint32_t pcol = tmem + (t ? C::COL_S1 : C::COL_S0);
-                                const uint32_t ocol = tmem + (t ? C::COL_O1 : C::COL_O0);
-                                const SmemDesc vd = smem_desc_parts(vb, C::HALF, 1024);
-                                tc_mma_ts_off<0>(ocol, pcol, vd, idesc_pv, first ? 0u : 1u);
-                                tc_mma_ts_off<2048>(ocol, pcol + 8, vd, idesc_pv, 1u);
-                                tc_mma_ts_off<4096>(ocol, pcol + 16, vd, idesc_pv, 1u);
-                                tc_mma_ts_off<6144>(ocol, pcol + 24, vd, idesc_pv, 1u);
-                                tc_mma_ts_off<8192>(ocol, pcol + 32, vd, idesc_pv, 1u);
-                                tc_mma_ts_off<10240>(ocol, pcol + 40, vd, idesc_pv, 1u);
-                                tc_mma_ts_off<12288>(ocol, pcol + 48, vd, idesc_pv, 1u);
-                                tc_mma_ts_off<14336>(ocol, pcol + 56, vd, idesc_pv, 1u);
-                                if (!prefill_uses(it, t, j + 1)) tc_commit(bar(BAR_OFULL + t));
-                            }
-                        }
-                        if (prefill_uses(it, t, j + 1)) {
                             tc_fence_after();
-                            issue_qk(t, sk1);
+                            issue_pv(0, vs, j == f0 ? 0u : 1u);
+                            if (j == l0) tc_commit(bar(BAR_OFULL + 0));
                         }
                     }
-                    if (!ok) break;
-                    if (j + 2 == it.n_kv) tc_commit(bar(BAR_QEMPTY));  // the item's last QK
-                    if (PASS != 1) tc_commit(bar(BAR_VEMPTY + sv));
-                    if (k_ready) tc_commit(bar(BAR_KEMPTY + sk1));
+                    if (j + 1 >= f0 && j + 1 <= l0) issue_qk(0, ks1);
+                    if (j >= f1 && j <= l1) {
+                        if (!mbar_wait(bar(BAR_PFULL + 1), (uint32_t)pc1 & 1u, p.status,
+                                       abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        ++pc1;
+                        if constexpr (PASS != 1) {
+                            if (j == f1 && !mbar_wait(bar(BAR_OEMPTY + 1),
+                                                      ((uint32_t)oc1 & 1u) ^ 1u, p.status,
+                                                      abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            issue_pv(1, vs, j == f1 ? 0u : 1u);
+                            if (j == l1) tc_commit(bar(BAR_OFULL + 1));
+                        }
+                    }
+                    if (j + 1 >= f1 && j + 1 <= l1) issue_qk(1, ks1);
+                    if (j + 2 == n_kv) tc_commit(bar(BAR_QEMPTY));  // the item's last QK
+                    if (PASS != 1) tc_commit(bar(BAR_VEMPTY + vs));
+                    if (more) tc_commit(bar(BAR_KEMPTY + ks1));
+                    if (++vs == C::SV) {
+                        vs = 0;
+                        vph ^= 1u;
+                    }
+                    ks = ks1;
+                    kph = kph1;
                 }
                 if (!ok) break;
-#pragma unroll
-                for (int t = 0; t < 2; ++t)
-                    if (it.valid[t]) ++oc[t];
-                kvc += it.n_kv;
+                if (it.valid[0]) ++oc0;
+                if (it.valid[1]) ++oc1;
             }
             // all issued MMAs complete before TMEM is released
             tc_commit(bar(BAR_DRAIN));
