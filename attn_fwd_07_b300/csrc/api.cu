@@ -62,11 +62,31 @@ attn_status_t launch_status() {
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
-// Shared-memory size attribute of every instantiation of the tensor-core prefill.
+// The tensor-core prefill's warpgroups trade registers with setmaxnreg; the counts they
+// ask for must fit in what the launch reserves per thread, or a raise would wait for
+// ever.  Checked per instantiation against the compiled register count.
+template <int D, bool PAGED, int PASS>
+cudaError_t prefill_regs_fit() {
+    using C = PrefillCfg<D>;
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, prefill_tc_kernel<D, PAGED, PASS>);
+    if (e != cudaSuccess) return e;
+    const long long have = (long long)a.numRegs * C::THREADS;
+    const long long need = (long long)C::REG_NEED;
+    return have >= need ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+// Shared-memory size attribute of every instantiation of the tensor-core prefill, and the
+// register check above.
 template <int D>
 cudaError_t prefill_attrs() {
     const int smem = (int)PrefillCfg<D>::SMEM;
     cudaError_t e;
+    if ((e = prefill_regs_fit<D, false, 0>()) != cudaSuccess ||
+        (e = prefill_regs_fit<D, true, 0>()) != cudaSuccess ||
+        (e = prefill_regs_fit<D, false, 1>()) != cudaSuccess ||
+        (e = prefill_regs_fit<D, false, 2>()) != cudaSuccess)
+        return e;
     if ((e = cudaFuncSetAttribute(prefill_tc_kernel<D, false, 0>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return e;

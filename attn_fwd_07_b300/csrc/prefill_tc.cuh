@@ -113,8 +113,10 @@ struct PrefillCfg {
     // TMEM columns
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
     static constexpr int THREADS = 512;
-    // per-thread registers after the split: softmax warpgroups / the other two
+    // per-thread registers after the split: softmax warpgroups / the other two, and the
+    // registers the split needs in all (at most what the launch reserves)
     static constexpr uint32_t REG_SOFTMAX = 184, REG_OTHER = 72;
+    static constexpr uint32_t REG_NEED = 128 * (2 * REG_SOFTMAX + 2 * REG_OTHER);
 };
 
 static_assert(PrefillCfg<128>::SMEM <= 227 * 1024, "prefill shared memory");
