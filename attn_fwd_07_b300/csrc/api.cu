@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <math.h>
 #include <mutex>
 #include <stdint.h>
@@ -25,6 +26,13 @@ using namespace attn07;
 // Device status word shared by every kernel of the library (per device).
 __device__ unsigned int g_attn_status;
 
+// Work counters of the tensor-core prefill, two per slot (next item, CTAs done).  A
+// launch takes the next slot in turn; it leaves its counters at zero when its last CTA
+// ends, so a slot is ready for reuse (a replayed graph reuses its launches' slots).
+// Launches in flight at the same time, on other streams, use other slots, up to 64.
+constexpr int kWorkSlots = 64;
+__device__ unsigned g_prefill_work[2 * kWorkSlots];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -33,7 +41,11 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     unsigned *status = nullptr;
+    unsigned *work = nullptr;  // g_prefill_work on this device
 };
+
+// prefill launches in this process, for the choice of work-counter slot
+std::atomic<unsigned> g_prefill_launches{0};
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -114,6 +126,8 @@ attn_status_t device_state(DeviceState **out) {
         void *sym = nullptr;
         if ((e = cudaGetSymbolAddress(&sym, g_attn_status)) != cudaSuccess) return cuda_fail(e);
         st.status = static_cast<unsigned *>(sym);
+        if ((e = cudaGetSymbolAddress(&sym, g_prefill_work)) != cudaSuccess) return cuda_fail(e);
+        st.work = static_cast<unsigned *>(sym);
         if ((e = cudaFuncSetAttribute(prefill_simt_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)prefill_simt_smem_bytes(kSimtMaxD))) != cudaSuccess)
@@ -237,6 +251,7 @@ attn_status_t launch_prefill_tc(const void *q, const void *k, const void *v, voi
     p.kv_lens = paged ? paged->kv_lens : nullptr;
     p.maxp = paged ? paged->maxp : 0;
     p.num_pages = paged ? paged->num_pages : 0;
+    p.work = st->work + 2 * (g_prefill_launches++ % kWorkSlots);
     // work items (pairs of query tiles); persistent CTAs, one per SM, walk them
     const long long items = p.head_pairs ? (long long)ntiles * (Hq / 2) * nseq
                                          : (long long)((ntiles + 1) / 2) * Hq * nseq;

@@ -18,13 +18,13 @@
 // two tiles' softmax runs while the tensor core works on the other tile
 // ("ping-pong").
 //
-// Persistent CTAs: one CTA per SM walks the items, round r taking item
-// r * gridDim.x + c (c = blockIdx.x; the order reverses every other round, which
-// evens out the heaviest-first list of causal items).  Each role keeps its own
-// position in the stream of items, so the next item's query tiles and first key
-// tiles load, and its first products run, while the previous item's output is
-// still being written: the per-item costs of a launch (set-up, first loads,
-// epilogue) are paid once per CTA.
+// Persistent CTAs: one CTA per SM.  Its producer warp takes item indices in order
+// (heaviest first) from the launch's work counter whenever it is ready for the
+// next one, decodes each item once, skips those with nothing to compute, and hands
+// the decoded items to the other roles through a small queue in shared memory.
+// Each role keeps its own ring positions and barrier phases across items, so the
+// next item's query tiles and first key tiles load, and its first products run,
+// while the previous item's output is still being written.
 //
 // Warp roles (512 threads, four warpgroups):
 //   warps 0-3    softmax of tile 0, one thread per query row (TMEM lane)
@@ -92,6 +92,10 @@ struct PrefillParams {
     const int32_t *page_table;  // [nseq, maxp]
     const int32_t *kv_lens;     // [nseq]
     int maxp, num_pages;
+    // the launch's work counters: work[0] hands out item indices in order, heaviest
+    // first, one at a time to whichever CTA asks; work[1] counts the CTAs that have
+    // finished, and the last one sets both back to zero for the next launch
+    unsigned *work;
 };
 
 template <int D>
@@ -107,7 +111,10 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_K = 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + SK * TILE;
     static constexpr uint32_t OFF_STATS = OFF_V + SV * TILE;  // [2][128] fp32: 1 / L per row
-    static constexpr uint32_t OFF_CTRL = OFF_STATS + 2 * 128 * 4;
+    // the queue of decoded work items the producer hands to the other roles
+    static constexpr int NQ = 4;
+    static constexpr uint32_t OFF_ITEMS = OFF_STATS + 2 * 128 * 4;
+    static constexpr uint32_t OFF_CTRL = OFF_ITEMS + NQ * 80;
     static constexpr uint32_t CTRL_BYTES = 512;
     static constexpr size_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
     // TMEM columns
@@ -139,7 +146,9 @@ enum : uint32_t {
     BAR_STATS = 26,   // +t: 1 / L of the item's rows written
     BAR_STATSE = 28,  // +t: ... and read by the epilogue
     BAR_DRAIN = 30,
-    BAR_COUNT = 31
+    BAR_IFULL = 31,   // +slot, slot < 4: item queue slot written
+    BAR_IEMPTY = 35,  // +slot: ... and read by every consumer
+    BAR_COUNT = 39
 };
 
 // One work item: the two query tiles, their rows, and the key tiles each needs.
@@ -147,8 +156,9 @@ struct PrefillItem {
     int head[2], row0[2], jlo[2], jhi[2];
     bool valid[2];
     int tok0, qlen, batch, kvlen, qoff, g, sq;
-    int J0, n_kv;  // key tiles J0 .. J0 + n_kv - 1 cover both tiles
+    int J0, n_kv;  // key tiles J0 .. J0 + n_kv - 1 cover both tiles (0: end of the queue)
 };
+static_assert(sizeof(PrefillItem) <= 80, "item queue slot");
 
 __device__ __forceinline__ int prefill_items(const PrefillParams &p) {
     const int units = (p.head_pairs ? p.Hq / 2 : p.Hq) * p.nseq;
@@ -156,10 +166,9 @@ __device__ __forceinline__ int prefill_items(const PrefillParams &p) {
     return nouter * units;
 }
 
-// Item of round r for this CTA: forward in even rounds, backward in odd ones.
-__device__ __forceinline__ int prefill_item_index(int r) {
-    const int G = (int)gridDim.x;
-    return r * G + ((r & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x);
+// The next item index of this launch from the work counter.
+__device__ __forceinline__ int prefill_next_item(const PrefillParams &p) {
+    return (int)atomicAdd(p.work, 1u);
 }
 
 // Decode item idx (heaviest query tiles first, heads fastest: a key/value head's
@@ -269,7 +278,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         record_status(p.status, kStatusBounds);
 
     const int n_items = prefill_items(p);
-    const int G = (int)gridDim.x;
 
     const uint32_t raw = smem_u32(pf_smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -277,6 +285,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     const uint32_t ctrl = base + C::OFF_CTRL;
     uint8_t *ctrl_ptr = base_ptr + C::OFF_CTRL;
     float *stats = reinterpret_cast<float *>(base_ptr + C::OFF_STATS);  // [2][128]
+    PrefillItem *items = reinterpret_cast<PrefillItem *>(base_ptr + C::OFF_ITEMS);
     auto bar = [&](uint32_t i) { return ctrl + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(ctrl_ptr + 8 * BAR_COUNT);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl_ptr + 8 * BAR_COUNT + 4);
@@ -304,6 +313,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             mbar_init(bar(BAR_STATSE + t), 4);
         }
         mbar_init(bar(BAR_DRAIN), 1);
+        for (int q = 0; q < C::NQ; ++q) {
+            mbar_init(bar(BAR_IFULL + q), 1);
+            // every consumer of the queue: the MMA thread, 8 softmax and 4 epilogue warps
+            mbar_init(bar(BAR_IEMPTY + q), 13);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -330,12 +344,37 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             const uint64_t pol_kv = policy_evict_last();
             int kvc = 0;                     // key tiles loaded so far (ring position)
             int nq = 0;                      // items whose query tiles were loaded
+            int npub = 0;                    // queue entries published (the end mark included)
             int issued_k = 0, issued_v = 0;  // ring positions issued
             bool ok = true;
-            for (int r = 0; ok && r * G < n_items; ++r) {
-                const int idx = prefill_item_index(r);
-                PrefillItem it;
-                if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, true, it)) continue;
+            // the next item with work, decoded: indices come from the launch's counter,
+            // heaviest first; the ones with nothing to compute are skipped here, once
+            auto fetch = [&](PrefillItem &dst) -> bool {
+                for (;;) {
+                    const int idx = prefill_next_item(p);
+                    if (idx >= n_items) return false;
+                    if (prefill_item<D, PAGED>(p, idx, true, dst)) return true;
+                }
+            };
+            PrefillItem it;
+            bool have = fetch(it);
+            for (;;) {
+                // hand the item (or the end of the queue) to the other roles
+                const int slot = npub % C::NQ;
+                if (!mbar_wait(bar(BAR_IEMPTY + slot), ((uint32_t)(npub / C::NQ) & 1u) ^ 1u,
+                               p.status, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (have)
+                    items[slot] = it;
+                else
+                    items[slot].n_kv = 0;
+                mbar_arrive(bar(BAR_IFULL + slot));
+                ++npub;
+                if (!have) break;
+                PrefillItem nx;
+                const bool have_nx = fetch(nx);
                 // both query tiles, once the previous item's QK products are done with theirs
                 if (!mbar_wait(bar(BAR_QEMPTY), ((uint32_t)nq & 1u) ^ 1u, p.status, abort_flag)) {
                     ok = false;
@@ -353,18 +392,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 }
                 ++nq;
                 // the next item's query tiles into L2 while this item runs
-                {
-                    const int idx2 = prefill_item_index(r + 1);
-                    PrefillItem nx;
-                    if (idx2 < n_items && prefill_item<D, PAGED>(p, idx2, false, nx)) {
+                if (have_nx) {
 #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            if (!nx.valid[t]) continue;
+                    for (int t = 0; t < 2; ++t) {
+                        if (!nx.valid[t]) continue;
 #pragma unroll
-                            for (int hf = 0; hf < C::NH; ++hf)
-                                tma_prefetch_4d(&tmQ, hf * 64, nx.head[t], nx.tok0 + nx.row0[t],
-                                                nx.batch);
-                        }
+                        for (int hf = 0; hf < C::NH; ++hf)
+                            tma_prefetch_4d(&tmQ, hf * 64, nx.head[t], nx.tok0 + nx.row0[t],
+                                            nx.batch);
                     }
                 }
                 const int npg = (it.kvlen + 15) / 16;  // pages holding this sequence's keys
@@ -446,6 +481,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     issued_v = kv + 1;
                 }
                 kvc += it.n_kv;
+                if (!ok) break;
+                it = nx;
+                have = have_nx;
             }
             if (*abort_flag) {
                 // let the copies already issued land before the CTA exits
@@ -513,10 +551,17 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             int pc0 = 0, pc1 = 0;        // P hand-offs consumed per tile
             int oc0 = 0, oc1 = 0;        // items per tile whose O was produced
             bool ok = true;
-            for (int r = 0; ok && r * G < n_items; ++r) {
-                const int idx = prefill_item_index(r);
-                PrefillItem it;
-                if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, false, it)) continue;
+            for (int ci = 0; ok; ++ci) {
+                // the next item from the producer's queue (an end mark closes it)
+                const int slot = ci % C::NQ;
+                if (!mbar_wait(bar(BAR_IFULL + slot), (uint32_t)(ci / C::NQ) & 1u, p.status,
+                               abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const PrefillItem it = items[slot];
+                mbar_arrive(bar(BAR_IEMPTY + slot));
+                if (it.n_kv == 0) break;
                 // steps [f_t, l_t] of the item use tile t (none for an invalid tile)
                 const int f0 = it.valid[0] ? it.jlo[0] - it.J0 : 1 << 30;
                 const int l0 = it.valid[0] ? it.jhi[0] - it.J0 : -1;
@@ -623,10 +668,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         int sc = 0;   // S tiles consumed (SFULL phases)
         int oc = 0;   // items of this tile (STATS / STATSE phases)
         bool ok = true;
-        for (int rr = 0; ok && rr * G < n_items; ++rr) {
-            const int idx = prefill_item_index(rr);
-            PrefillItem it;
-            if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, false, it)) continue;
+        for (int ci = 0; ok; ++ci) {
+            // the next item from the producer's queue (an end mark closes it)
+            const int slot = ci % C::NQ;
+            ok = mbar_wait(bar(BAR_IFULL + slot), (uint32_t)(ci / C::NQ) & 1u, p.status, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            const PrefillItem it = items[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_IEMPTY + slot));
+            if (it.n_kv == 0) break;
             if (!it.valid[t]) continue;
             const int j_first = it.jlo[t];
             const int n_mine = it.jhi[t] - j_first + 1;
@@ -852,17 +905,27 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     } else {
         // ============================ epilogue: thread = query row of both tiles
         setmaxnreg_dec<C::REG_OTHER>();
-        if constexpr (PASS != 1) {
+        {
             const int r = threadIdx.x & 127;       // row in tile = TMEM lane
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
             int oc[2] = {0, 0};
             bool ok = true;
-            for (int rr = 0; ok && rr * G < n_items; ++rr) {
-                const int idx = prefill_item_index(rr);
-                PrefillItem it;
-                if (idx >= n_items || !prefill_item<D, PAGED>(p, idx, false, it)) continue;
+            for (int ci = 0; ok; ++ci) {
+                // the next item from the producer's queue (an end mark closes it)
+                const int slot = ci % C::NQ;
+                ok = mbar_wait(bar(BAR_IFULL + slot), (uint32_t)(ci / C::NQ) & 1u, p.status,
+                               abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                const PrefillItem it = items[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_IEMPTY + slot));
+                if (it.n_kv == 0) break;
+                // (the statistics pass writes no output)
 #pragma unroll 1
-                for (int t = 0; t < 2; ++t) {
+                for (int t = 0; t < 2 && PASS != 1; ++t) {
                     if (!it.valid[t]) continue;
                     ok = mbar_wait(bar(BAR_STATS + t), (uint32_t)oc[t] & 1u, p.status, abort_flag);
                     const float inv = stats[t * 128 + r];
@@ -914,6 +977,16 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    // every role of this CTA is done with the work counter; the last CTA to get here
+    // sets the launch's counters back to zero
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.work + 1, 1u) == gridDim.x - 1) {
+            __threadfence();
+            p.work[0] = 0u;
+            p.work[1] = 0u;
+        }
     }
 }
 
