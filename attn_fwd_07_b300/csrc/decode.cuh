@@ -192,24 +192,43 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
             prefetch_tmap(&tmV);
         }
         const uint64_t pol = policy_evict_first();
-        // find the sequence holding global page p0
+        // find the sequence holding global page p0: 32 sequences at a time, the lanes'
+        // page counts summed by a prefix scan and the first lane past p0 taken
         int b = 0;
         long long seq_start = 0;  // global index of sequence b's first page
         int np_b = 0;
-        if (n_iter > 0) {
-            for (;;) {
-                np_b = dec_pages_of(p, b);
-                if (seq_start + np_b > p0) break;
-                seq_start += np_b;
-                ++b;
+        bool found = n_iter == 0;
+        for (int b0 = 0; !found && b0 < p.B; b0 += 32) {
+            const int np_l = (b0 + lane < p.B) ? dec_pages_of(p, b0 + lane) : 0;
+            long long incl = np_l;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
             }
+            const unsigned hit = __ballot_sync(0xffffffffu, seq_start + incl > p0);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                b = b0 + l;
+                np_b = __shfl_sync(0xffffffffu, np_l, l);
+                seq_start += __shfl_sync(0xffffffffu, incl, l) - np_b;
+                found = true;
+            } else {
+                seq_start += __shfl_sync(0xffffffffu, incl, 31);
+            }
+        }
+        // (the page counts summed above cover page p0, so this holds unless seq_lens
+        // changed under the kernel; the ring is then left unfilled and the consumers'
+        // bounded waits end the launch with an error)
+        if (!found) {
+            if (lane == 0) record_status(p.status, kStatusBounds);
         }
         int lp = (int)(p0 - seq_start);   // page of sequence b, counted from its first
         int fp_b = n_iter > 0 ? dec_first_token(p, b) / kDecPage : 0;  // first logical page
         int ids_base = -1;                // logical page of ids[lane] batch start
         int my_id = 0;
         const uint32_t tx = stage_bytes;
-        for (int it = 0; it < n_iter; ++it) {
+        for (int it = 0; found && it < n_iter; ++it) {
             // advance to the next non-empty sequence when the current one is done
             while (lp >= np_b) {
                 ++b;

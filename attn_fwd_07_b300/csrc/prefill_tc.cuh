@@ -20,7 +20,7 @@
 //
 // Persistent CTAs: one CTA per SM.  Its producer warp takes item indices in order
 // (heaviest first) from the launch's work counter whenever it is ready for the
-// next one, decodes each item once, skips those with nothing to compute, and hands
+// next one (the first is the CTA's own index), decodes each item once, skips those with nothing to compute, and hands
 // the decoded items to the other roles through a small queue in shared memory.
 // Each role keeps its own ring positions and barrier phases across items, so the
 // next item's query tiles and first key tiles load, and its first products run,
@@ -111,8 +111,10 @@ struct PrefillCfg {
     static constexpr uint32_t OFF_K = 2 * TILE;
     static constexpr uint32_t OFF_V = OFF_K + SK * TILE;
     static constexpr uint32_t OFF_STATS = OFF_V + SV * TILE;  // [2][128] fp32: 1 / L per row
-    // the queue of decoded work items the producer hands to the other roles
+    // the queue of decoded work items the producer hands to the other roles, and how
+    // many key tiles before the end of an item the producer claims the next one
     static constexpr int NQ = 4;
+    static constexpr int CLAIM = 2;
     static constexpr uint32_t OFF_ITEMS = OFF_STATS + 2 * 128 * 4;
     static constexpr uint32_t OFF_CTRL = OFF_ITEMS + NQ * 80;
     static constexpr uint32_t CTRL_BYTES = 512;
@@ -166,18 +168,83 @@ __device__ __forceinline__ int prefill_items(const PrefillParams &p) {
     return nouter * units;
 }
 
-// The next item index of this launch from the work counter.
+// The next item index of this launch from the work counter.  CTA c's first item is
+// item c (no counter access on the way to the first loads); the counter hands out
+// the items from gridDim.x on.
 __device__ __forceinline__ int prefill_next_item(const PrefillParams &p) {
-    return (int)atomicAdd(p.work, 1u);
+    return (int)gridDim.x + (int)atomicAdd(p.work, 1u);
 }
 
-// Decode item idx (heaviest query tiles first, heads fastest: a key/value head's
-// query heads run together and share its K/V tiles in L2).  Returns false when it
-// has nothing to compute.  With `report`, records the bounds errors it finds (one
-// role reports, so that each is recorded once).
+// The items are numbered heaviest query tiles first, heads fastest (a key/value
+// head's query heads run together and share its K/V tiles in L2): item idx is head
+// unit idx % hunits of block idx / hunits, and block b is query-tile level
+// nouter - 1 - b / nseq of sequence b % nseq.  Whether an item has work depends on
+// its block only.
+
+// Whether sequence sq's sizes are valid (packed tokens inside [0, total); a paged
+// sequence's cache holds its queries and fits its page-table row), and the rows its
+// queries take: [tok0, tok0 + qlen), keys [0, kvlen), query i at position qoff + i.
+template <bool PAGED>
+__device__ __forceinline__ bool prefill_seq(const PrefillParams &p, int sq, int &tok0, int &qlen,
+                                            int &kvlen, int &qoff) {
+    if (p.cu_seqlens) {
+        tok0 = p.cu_seqlens[sq];
+        const int tend = p.cu_seqlens[sq + 1];
+        qlen = tend - tok0;
+        if (tok0 < 0 || tend < tok0 || tend > p.total) return false;
+    } else {
+        tok0 = 0;
+        qlen = p.N;
+    }
+    kvlen = qlen;
+    qoff = 0;
+    if constexpr (PAGED) {
+        kvlen = p.kv_lens[sq];
+        qoff = kvlen - qlen;
+        if (qoff < 0 || kvlen > p.maxp * 16) return false;
+    }
+    return true;
+}
+
+// Records the bounds errors of sequence sq: sizes outside the rules above (nothing of
+// the sequence is read or written), or more packed rows than the launch's tiles
+// cover (only those rows are done).  Each sequence is checked by one lane of one CTA.
 template <int D, bool PAGED>
-__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int idx, bool report,
-                                             PrefillItem &it) {
+__device__ __forceinline__ void prefill_check_seq(const PrefillParams &p, int sq) {
+    int qlen = p.N;
+    if (p.cu_seqlens) {
+        const int tok0 = p.cu_seqlens[sq];
+        const int tend = p.cu_seqlens[sq + 1];
+        qlen = tend - tok0;
+        if (tok0 < 0 || tend < tok0 || tend > p.total) {
+            record_status(p.status, kStatusBounds);
+            return;
+        }
+        if (qlen > (p.tile0 + p.ntiles) * PrefillCfg<D>::BM) record_status(p.status, kStatusBounds);
+    }
+    if constexpr (PAGED) {
+        // (a sequence with no queries in this call is not checked against its cache)
+        const int kvlen = p.kv_lens[sq];
+        if (qlen > 0 && (kvlen - qlen < 0 || kvlen > p.maxp * 16))
+            record_status(p.status, kStatusBounds);
+    }
+}
+
+// Whether block b has work.
+template <int D, bool PAGED>
+__device__ __forceinline__ bool prefill_block_has_work(const PrefillParams &p, int b) {
+    using C = PrefillCfg<D>;
+    const int nouter = p.head_pairs ? p.ntiles : (p.ntiles + 1) / 2;
+    const int outer = nouter - 1 - b / p.nseq;
+    int tok0, qlen, kvlen, qoff;
+    if (!prefill_seq<PAGED>(p, b % p.nseq, tok0, qlen, kvlen, qoff)) return false;
+    const int row0 = (p.tile0 + (p.head_pairs ? outer : 2 * outer)) * C::BM;
+    return row0 < min(qlen, (p.tile0 + p.ntiles) * C::BM);
+}
+
+// Decode item idx; returns false when it has nothing to compute.
+template <int D, bool PAGED>
+__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int idx, PrefillItem &it) {
     using C = PrefillCfg<D>;
     const int hunits = p.head_pairs ? p.Hq / 2 : p.Hq;
     const int units = hunits * p.nseq;
@@ -186,36 +253,9 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int idx, bo
     const int rem = idx % units;
     const int hu = rem % hunits;
     const int sq = rem / hunits;
-    const bool seq_first = outer == nouter - 1 && hu == 0;  // one item per sequence
-    // query rows [0, qlen) of this sequence sit at positions qoff + i; keys at [0, kvlen)
-    int tok0, qlen, batch;
-    if (p.cu_seqlens) {
-        tok0 = p.cu_seqlens[sq];
-        const int tend = p.cu_seqlens[sq + 1];
-        qlen = tend - tok0;
-        batch = 0;
-        // a sequence whose tokens leave [0, total) is skipped, nothing of it read or
-        // written; one longer than the launch's tiles has only those rows done
-        if (tok0 < 0 || tend < tok0 || tend > p.total) {
-            if (report && seq_first) record_status(p.status, kStatusBounds);
-            return false;
-        }
-        if (report && seq_first && qlen > (p.tile0 + p.ntiles) * C::BM)
-            record_status(p.status, kStatusBounds);
-    } else {
-        tok0 = 0;
-        qlen = p.N;
-        batch = sq;
-    }
-    int kvlen = qlen, qoff = 0;
-    if constexpr (PAGED) {
-        kvlen = p.kv_lens[sq];
-        qoff = kvlen - qlen;
-        if (qoff < 0 || kvlen > p.maxp * 16) {  // the sequence's sizes are invalid
-            if (report && outer == nouter - 1 && qlen > 0) record_status(p.status, kStatusBounds);
-            return false;
-        }
-    }
+    int tok0, qlen, kvlen, qoff;
+    if (!prefill_seq<PAGED>(p, sq, tok0, qlen, kvlen, qoff)) return false;
+    const int batch = p.cu_seqlens ? 0 : sq;
     if (p.head_pairs) {
         it.head[0] = 2 * hu;
         it.head[1] = 2 * hu + 1;
@@ -336,6 +376,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
     setmaxnreg_dec<C::REG_OTHER>();
     if (warp == 12) {
         // ============================ TMA producer
+        // every packed or paged sequence's sizes are checked once per launch, the
+        // sequences spread over the CTAs' producer warps
+        if (p.cu_seqlens != nullptr || PAGED)
+            for (int sq = (int)blockIdx.x * 32 + lane; sq < p.nseq; sq += (int)gridDim.x * 32)
+                prefill_check_seq<D, PAGED>(p, sq);
         if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
@@ -349,15 +394,29 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
             bool ok = true;
             // the next item with work, decoded: indices come from the launch's counter,
             // heaviest first; the ones with nothing to compute are skipped here, once
-            auto fetch = [&](PrefillItem &dst) -> bool {
+            // An item without work belongs to a block without work (a query-tile level
+            // past its sequence's end, or a sequence whose sizes are invalid): the blocks
+            // after it are checked here, up to a valid one, and the counter is moved past
+            // the ones between (none of their items has work), so that no CTA claims
+            // them one at a time.
+            const int hunits = p.head_pairs ? p.Hq / 2 : p.Hq;
+            const int n_blocks = n_items / hunits;
+            auto fetch = [&](PrefillItem &dst, bool first) -> bool {
+                int idx = first ? (int)blockIdx.x : prefill_next_item(p);
                 for (;;) {
-                    const int idx = prefill_next_item(p);
                     if (idx >= n_items) return false;
-                    if (prefill_item<D, PAGED>(p, idx, true, dst)) return true;
+                    if (prefill_item<D, PAGED>(p, idx, dst)) return true;
+                    int b = idx / hunits + 1;
+                    for (int k = 0; k < 64 && b < n_blocks && !prefill_block_has_work<D, PAGED>(p, b);
+                         ++k)
+                        ++b;
+                    const long long target = (long long)b * hunits - (long long)gridDim.x;
+                    if (target > 0) atomicMax(p.work, (unsigned)target);
+                    idx = prefill_next_item(p);
                 }
             };
             PrefillItem it;
-            bool have = fetch(it);
+            bool have = fetch(it, true);
             for (;;) {
                 // hand the item (or the end of the queue) to the other roles
                 const int slot = npub % C::NQ;
@@ -373,8 +432,6 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 mbar_arrive(bar(BAR_IFULL + slot));
                 ++npub;
                 if (!have) break;
-                PrefillItem nx;
-                const bool have_nx = fetch(nx);
                 // both query tiles, once the previous item's QK products are done with theirs
                 if (!mbar_wait(bar(BAR_QEMPTY), ((uint32_t)nq & 1u) ^ 1u, p.status, abort_flag)) {
                     ok = false;
@@ -391,17 +448,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                                     it.batch, pol_q);
                 }
                 ++nq;
-                // the next item's query tiles into L2 while this item runs
-                if (have_nx) {
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (!nx.valid[t]) continue;
-#pragma unroll
-                        for (int hf = 0; hf < C::NH; ++hf)
-                            tma_prefetch_4d(&tmQ, hf * 64, nx.head[t], nx.tok0 + nx.row0[t],
-                                            nx.batch);
-                    }
-                }
+                // the next item is claimed when this one's last CLAIM key tiles are being
+                // loaded: late enough that the end of the launch evens out, early enough
+                // that its query tiles are in L2 when they are needed
+                PrefillItem nx;
+                bool have_nx = false;
+                const int j_claim = max(0, it.n_kv - C::CLAIM);
                 const int npg = (it.kvlen + 15) / 16;  // pages holding this sequence's keys
                 // PAGED: page ids of key tile J0 + j (eight 16-token pages), read one tile
                 // ahead so the loads overlap the waits; -1 past the sequence
@@ -457,6 +509,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                         }
                     }
                     issued_k = kv + 1;
+                    if (j == j_claim) {
+                        have_nx = fetch(nx, false);
+                        if (have_nx) {
+#pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                if (!nx.valid[t]) continue;
+#pragma unroll
+                                for (int hf = 0; hf < C::NH; ++hf)
+                                    tma_prefetch_4d(&tmQ, hf * 64, nx.head[t],
+                                                    nx.tok0 + nx.row0[t], nx.batch);
+                            }
+                        }
+                    }
                     if constexpr (PASS == 1) continue;  // the statistics need no values
                     const int sv = kv % C::SV;
                     if (!mbar_wait(bar(BAR_VEMPTY + sv), ((uint32_t)(kv / C::SV) & 1u) ^ 1u,
@@ -908,6 +973,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         {
             const int r = threadIdx.x & 127;       // row in tile = TMEM lane
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
             int oc[2] = {0, 0};
             bool ok = true;
             for (int ci = 0; ok; ++ci) {
@@ -945,20 +1011,30 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                     __nv_bfloat16 *orow =
                         p.o + ((p.cu_seqlens ? tok : (long long)it.batch * p.N + qpos) * p.Hq +
                                it.head[t]) * D;
+                    // 32 columns per TMEM wait; each 16 columns (32 bytes of the row) go out
+                    // in one 32-byte store when O is 32-byte aligned (rows are D * 2 bytes)
 #pragma unroll
-                    for (int c = 0; c < D; c += 16) {
-                        uint32_t orr[16];
-                        tmem_ld16(ocol + c, orr);
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t orr[2][16];
+                        tmem_ld16(ocol + c, orr[0]);
+                        tmem_ld16(ocol + c + 16, orr[1]);
                         tc_wait_ld();
-                        uint32_t pkd[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            pkd[e] = pack_bf16(__uint_as_float(orr[2 * e]) * inv,
-                                               __uint_as_float(orr[2 * e + 1]) * inv);
-                        if (row_ok) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
-                            dst[0] = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
-                            dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t pkd[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                pkd[e] = pack_bf16(__uint_as_float(orr[h][2 * e]) * inv,
+                                                   __uint_as_float(orr[h][2 * e + 1]) * inv);
+                            if (row_ok) {
+                                if (o32) {
+                                    stg256(orow + c + 16 * h, pkd);
+                                } else {
+                                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c + 16 * h);
+                                    dst[0] = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+                                    dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
+                                }
+                            }
                         }
                     }
                     // O_t is out of TMEM: the next item's first product may overwrite it

@@ -322,6 +322,14 @@ __device__ __forceinline__ void tc_mma_ts_off(uint32_t d_tmem, uint32_t a_tmem, 
 
 // ------------------------------------------------------------------ shared memory
 
+// 32-byte global store (sm_100 family); addr must be 32-byte aligned
+__device__ __forceinline__ void stg256(void *addr, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -239,3 +239,26 @@ def test_chunk_cu_seqlens_past_the_query_count(oracle):
     lg = f32(lse)[rows[:, 1], rows[:, 0]]
     assert_close(errors(og, o_ref, lg, l_ref))
     assert untouched(o, lse, 100, 150)
+
+
+# ---------------------------------------------------------------- output alignment
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_output_at_a_16_byte_offset(d):
+    """The prefill writes O rows with 32-byte stores when O is 32-byte aligned and with
+    16-byte stores otherwise (the interface asks for 16-byte alignment).  An O that
+    starts 16 bytes past a 32-byte boundary gets the same values, and its guard bands
+    stay untouched."""
+    w = inputs.dense(2, 300, 4, 2, d, 5401)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    o_ref, lse_ref = A.attn_fwd(q, k, v, True, w.scale)
+    n = q.numel()
+    buf = torch.full((PAD + 8 + n + PAD,), SENTINEL_BF16, dtype=torch.bfloat16, device="cuda")
+    o = buf[PAD + 8:PAD + 8 + n].view(q.shape)           # 16 bytes past a 32-byte boundary
+    assert o.data_ptr() % 32 == 16
+    o2, lse2 = A.attn_fwd(q, k, v, True, w.scale, o=o)
+    torch.cuda.synchronize()
+    assert A.attn_get_device_status() == 0
+    assert torch.equal(o2, o_ref) and torch.equal(lse2, lse_ref)
+    assert bool((buf[:PAD + 8].float() == SENTINEL_BF16).all())
+    assert bool((buf[PAD + 8 + n:].float() == SENTINEL_BF16).all())
