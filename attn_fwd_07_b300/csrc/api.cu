@@ -517,9 +517,9 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     const int G = ctas > 0 ? ctas : st->sms * ctas_per_sm;
     const size_t smem = dec_smem_bytes(Hkv, d, stages, fp8);
     if (fp8)
-        decode_split_kernel<true><<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
+        decode_split_kernel<true><<<G, 32 * Hkv, smem, cs>>>(p, mk, mv);
     else
-        decode_split_kernel<false><<<G, 32 * (Hkv + 1), smem, cs>>>(p, mk, mv);
+        decode_split_kernel<false><<<G, 32 * Hkv, smem, cs>>>(p, mk, mv);
     if ((s = launch_status()) != ATTN_OK) return s;
     // the merge as a programmatic dependent of the split kernel: it is scheduled while
     // the split kernel's last CTAs run and waits on the device for their results, which

@@ -25,10 +25,14 @@
 //       (the same rescaling rule, applied across key ranges), writing bf16 O
 //       and fp32 LSE.
 //
-// Data movement: a TMA producer warp copies each page -- all key/value heads,
-// 16 tokens -- into a multi-stage shared-memory ring, as 128-byte-swizzled
-// boxes of [head][token][64 dims] so that each head's 16 token rows are
-// conflict-free for ldmatrix.  One consumer warp per key/value head computes
+// Data movement: TMA copies each page -- all key/value heads, 16 tokens -- into
+// a multi-stage shared-memory ring, as 128-byte-swizzled boxes of
+// [head][token][64 dims] so that each head's 16 token rows are conflict-free for
+// ldmatrix.  There is no producer warp: every warp walks the CTA's page stream,
+// the ring is kept S pages ahead, and the warp that releases a page's stage last
+// refills it with the page S further on (its id read while the page was being
+// attended).  The CTA is one warp per key/value head, so two CTAs of the FP8
+// kernel fit an SM at 128 registers a thread.  Each warp computes
 // S = q K^T and O += P V for its Hq/Hkv query heads with mma.sync m16n8k16
 // (bf16 in, fp32 accumulate; the query heads fill the first rows of the
 // 16-row tile).  The decode is bound by device-memory bandwidth: the
@@ -69,13 +73,14 @@ struct DecodeStageMeta {
     int last;     // last page of a segment
 };
 
-static_assert(sizeof(DecodeStageMeta) * kDecMaxStages <= 256, "stage metadata must fit");
+static_assert(sizeof(DecodeStageMeta) * kDecMaxStages <= 160, "stage metadata must fit");
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base):
 //   stage s:  bf16 cache: K half 0 .. K half (d/64 - 1), V half 0 .. V half (d/64 - 1),
 //             each [Hkv][16][64] bf16 = Hkv * 2048 bytes;
 //             FP8 cache (d = 128): K, then V, each [Hkv][16][128] bytes = Hkv * 2048
-//   then full[kDecMaxStages], empty[kDecMaxStages] mbarriers, meta, scalars (1 KB).
+//   then full[kDecMaxStages], empty[kDecMaxStages] mbarriers, meta, release counts,
+//   scalars (1 KB).
 __host__ __device__ inline uint32_t dec_half_bytes(int Hkv) { return (uint32_t)Hkv * 16u * 128u; }
 __host__ __device__ inline uint32_t dec_stage_bytes(int Hkv, int d, bool fp8) {
     return 2u * (fp8 ? 1u : (uint32_t)(d / 64)) * dec_half_bytes(Hkv);
@@ -130,7 +135,7 @@ __host__ __device__ __forceinline__ bool dec_range_nonempty(long long c, long lo
 // them to f16 (exact) and runs the products with f16 operands; per-head scales
 // multiply the scores and the output.
 template <bool FP8>
-__global__ void __launch_bounds__(32 * (kDecMaxHkv + 1), FP8 ? 2 : 1)
+__global__ void __launch_bounds__(32 * kDecMaxHkv, FP8 ? 2 : 1)
 decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ uint8_t dec_smem_raw[];
@@ -144,9 +149,12 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
     const int nhalf = FP8 ? 1 : p.d / 64;   // TMA boxes per tensor and page
     const uint32_t ctrl = base + (uint32_t)S * stage_bytes;
     uint8_t *ctrl_ptr = base_ptr + (size_t)S * stage_bytes;
-    // control block: full[8] @0, empty[8] @64, meta[8] @128, scalars @384
+    // control block: full[8] @0, empty[8] @64, meta[8] @128, released[8] @288,
+    // n_issued[8] @320, scalars @384
     const uint32_t full0 = ctrl, empty0 = ctrl + 64;
     DecodeStageMeta *meta = reinterpret_cast<DecodeStageMeta *>(ctrl_ptr + 128);
+    int *released = reinterpret_cast<int *>(ctrl_ptr + 288);   // warps done with a stage
+    int *n_issued = reinterpret_cast<int *>(ctrl_ptr + 320);   // pages issued into a stage
     volatile int *abort_flag = reinterpret_cast<volatile int *>(ctrl_ptr + 384);
     int *shared_n = reinterpret_cast<int *>(ctrl_ptr + 388);
 
@@ -161,122 +169,124 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, Hkv);
+            released[s] = 0;
+            n_issued[s] = 0;
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
 
-    // ---- this CTA's page range (computed by the producer warp, published)
-    long long T = 0;  // total pages of all sequences
-    if (warp == Hkv) {
-        for (int b0 = 0; b0 < p.B; b0 += 32) {
-            int np = (b0 + lane < p.B) ? dec_pages_of(p, b0 + lane) : 0;
+    // ---- the total page count T: every warp sums it (a few loads per 32 sequences),
+    // so that each can find this CTA's first page below without waiting for another
+    long long T = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        int np = (b0 + lane < p.B) ? dec_pages_of(p, b0 + lane) : 0;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) np += __shfl_xor_sync(0xffffffffu, np, o);
-            T += np;
+        for (int o = 16; o > 0; o >>= 1) np += __shfl_xor_sync(0xffffffffu, np, o);
+        T += np;
+    }
+    const long long p0 = (long long)blockIdx.x * T / G;
+    const int n_iter = (int)((long long)(blockIdx.x + 1) * T / G - p0);
+    (void)shared_n;
+
+    // ---- the page stream of this CTA: pages p0 .. p0 + n_iter - 1 in sequence order.
+    // Every warp keeps a cursor on it; the ring is filled S pages ahead of the pages
+    // being attended, the stage of page it being refilled with page it + S by the warp
+    // that releases it last, with the id and sizes its own cursor holds.
+    // find the sequence holding global page p0: 32 sequences at a time, the lanes'
+    // page counts summed by a prefix scan and the first lane past p0 taken
+    int cb = 0;               // cursor: sequence
+    long long seq_start = 0;  // global index of sequence cb's first page
+    int cnp = 0;              // pages of sequence cb
+    bool found = n_iter == 0;
+    for (int b0 = 0; !found && b0 < p.B; b0 += 32) {
+        const int np_l = (b0 + lane < p.B) ? dec_pages_of(p, b0 + lane) : 0;
+        long long incl = np_l;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
-        if (lane == 0) {
-            const long long p0 = (long long)blockIdx.x * T / G;
-            const long long p1 = (long long)(blockIdx.x + 1) * T / G;
-            *shared_n = (int)(p1 - p0);
+        const unsigned hit = __ballot_sync(0xffffffffu, seq_start + incl > p0);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            cb = b0 + l;
+            cnp = __shfl_sync(0xffffffffu, np_l, l);
+            seq_start += __shfl_sync(0xffffffffu, incl, l) - cnp;
+            found = true;
+        } else {
+            seq_start += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
-    __syncthreads();
-    const int n_iter = *shared_n;
-
-    if (warp == Hkv) {
-        // ================= producer: page ids -> TMA into the ring
-        const long long p0 = (long long)blockIdx.x * T / G;
-        if (lane == 0) {
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
+    // (the page counts summed above cover page p0, so this holds unless seq_lens
+    // changed under the kernel; the ring is then left unfilled and the bounded waits
+    // end the launch with an error)
+    if (!found && warp == 0 && lane == 0) record_status(p.status, kStatusBounds);
+    int clp = (int)(p0 - seq_start);                               // cursor: page of cb
+    int cfp = found && n_iter > 0 ? dec_first_token(p, cb) / kDecPage : 0;  // first logical page
+    int cit = 0;                                                   // cursor: page index
+    // moves the cursor to the next page of the stream (empty sequences skipped)
+    auto advance = [&]() {
+        ++clp;
+        ++cit;
+        while (cit < n_iter && clp >= cnp && cb + 1 < p.B) {
+            ++cb;
+            clp = 0;
+            cnp = dec_pages_of(p, cb);
+            cfp = dec_first_token(p, cb) / kDecPage;
         }
-        const uint64_t pol = policy_evict_first();
-        // find the sequence holding global page p0: 32 sequences at a time, the lanes'
-        // page counts summed by a prefix scan and the first lane past p0 taken
-        int b = 0;
-        long long seq_start = 0;  // global index of sequence b's first page
-        int np_b = 0;
-        bool found = n_iter == 0;
-        for (int b0 = 0; !found && b0 < p.B; b0 += 32) {
-            const int np_l = (b0 + lane < p.B) ? dec_pages_of(p, b0 + lane) : 0;
-            long long incl = np_l;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
+    };
+    // the cursor's page id (read by lane 0; -1 past the stream, or off the sequence's
+    // pages if seq_lens changed under the kernel)
+    auto cursor_id = [&]() -> int {
+        return (cit < n_iter && clp < cnp) ? p.page_table[(long long)cb * p.maxp + cfp + clp]
+                                           : -1;
+    };
+    const uint64_t pol = policy_evict_first();
+    // page `cit` of the stream (id pid) into its stage: its sizes into the stage's
+    // metadata, then K and V by TMA (a page id out of range is reported and the stage
+    // handed over empty)
+    auto issue = [&](int pid) {
+        const int s = cit % S;
+        const bool last_of_seq = (clp == cnp - 1);
+        const bool valid = (unsigned)pid < (unsigned)p.num_pages;
+        DecodeStageMeta mt;
+        mt.b = cb;
+        mt.ntok = valid ? (last_of_seq ? dec_len(p, cb) - (cfp + clp) * kDecPage : kDecPage) : 0;
+        mt.lo = clp == 0 ? dec_first_token(p, cb) - cfp * kDecPage : 0;
+        mt.first = (cit == 0 || clp == 0) ? 1 : 0;
+        mt.last = (cit == n_iter - 1 || last_of_seq) ? 1 : 0;
+        meta[s] = mt;
+        ++n_issued[s];
+        const uint32_t dst = base + (uint32_t)s * stage_bytes;
+        if (valid) {
+            mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
+            for (int hf = 0; hf < nhalf; ++hf) {
+                tma_load_4d(dst + hf * half_bytes, &tmK, full0 + 8 * s, hf * 64, 0, 0, pid, pol);
+                tma_load_4d(dst + (nhalf + hf) * half_bytes, &tmV, full0 + 8 * s, hf * 64, 0, 0,
+                            pid, pol);
             }
-            const unsigned hit = __ballot_sync(0xffffffffu, seq_start + incl > p0);
-            if (hit) {
-                const int l = __ffs(hit) - 1;
-                b = b0 + l;
-                np_b = __shfl_sync(0xffffffffu, np_l, l);
-                seq_start += __shfl_sync(0xffffffffu, incl, l) - np_b;
-                found = true;
-            } else {
-                seq_start += __shfl_sync(0xffffffffu, incl, 31);
-            }
+        } else {
+            record_status(p.status, kStatusBounds);
+            mbar_arrive(full0 + 8 * s);
         }
-        // (the page counts summed above cover page p0, so this holds unless seq_lens
-        // changed under the kernel; the ring is then left unfilled and the consumers'
-        // bounded waits end the launch with an error)
-        if (!found) {
-            if (lane == 0) record_status(p.status, kStatusBounds);
-        }
-        int lp = (int)(p0 - seq_start);   // page of sequence b, counted from its first
-        int fp_b = n_iter > 0 ? dec_first_token(p, b) / kDecPage : 0;  // first logical page
-        int ids_base = -1;                // logical page of ids[lane] batch start
-        int my_id = 0;
-        const uint32_t tx = stage_bytes;
-        for (int it = 0; found && it < n_iter; ++it) {
-            // advance to the next non-empty sequence when the current one is done
-            while (lp >= np_b) {
-                ++b;
-                lp = 0;
-                np_b = dec_pages_of(p, b);
-                fp_b = dec_first_token(p, b) / kDecPage;
-                ids_base = -1;
-            }
-            if (ids_base < 0 || lp >= ids_base + 32) {
-                ids_base = lp;
-                my_id = (lp + lane < np_b)
-                            ? p.page_table[(long long)b * p.maxp + fp_b + lp + lane] : 0;
-            }
-            const int pid = __shfl_sync(0xffffffffu, my_id, lp - ids_base);
-            const int s = it % S;
-            const uint32_t par = ((uint32_t)(it / S) & 1u) ^ 1u;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(empty0 + 8 * s, par, p.status, abort_flag);
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            const bool last_of_seq = (lp == np_b - 1);
-            if (lane == 0) {
-                const bool valid = (unsigned)pid < (unsigned)p.num_pages;
-                DecodeStageMeta mt;
-                mt.b = b;
-                mt.ntok = valid ? (last_of_seq ? dec_len(p, b) - (fp_b + lp) * kDecPage : kDecPage)
-                                : 0;
-                mt.lo = lp == 0 ? dec_first_token(p, b) - fp_b * kDecPage : 0;
-                mt.first = (it == 0 || lp == 0) ? 1 : 0;
-                mt.last = (it == n_iter - 1 || last_of_seq) ? 1 : 0;
-                meta[s] = mt;
-                const uint32_t dst = base + (uint32_t)s * stage_bytes;
-                if (valid) {
-                    mbar_arrive_expect_tx(full0 + 8 * s, tx);
-                    for (int hf = 0; hf < nhalf; ++hf) {
-                        tma_load_4d(dst + hf * half_bytes, &tmK, full0 + 8 * s, hf * 64, 0, 0,
-                                    pid, pol);
-                        tma_load_4d(dst + (nhalf + hf) * half_bytes, &tmV, full0 + 8 * s,
-                                    hf * 64, 0, 0, pid, pol);
-                    }
-                } else {
-                    record_status(p.status, kStatusBounds);
-                    mbar_arrive(full0 + 8 * s);
+    };
+    __syncthreads();  // barriers initialised
+    if (found) {
+        // the first S pages: warp 0 issues them; every warp moves its cursor past them
+        for (int i = 0; i < S && cit < n_iter; ++i) {
+            if (warp == 0 && lane == 0) {
+                if (i == 0) {
+                    prefetch_tmap(&tmK);
+                    prefetch_tmap(&tmV);
                 }
+                issue(cursor_id());
             }
-            ++lp;
+            advance();
         }
-    } else if (warp < Hkv) {
+    }
+
+    {
         // ================= consumers: warp g serves kv head g
         const int g = warp;
         const int Gq = p.Hq / Hkv;             // query heads per kv head (<= 8)
@@ -298,9 +308,12 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         float m_run = -INFINITY, l_run = 0.f, q_run = 0.f;
         int cur_b = 0;
 
-        for (int it = 0; it < n_iter; ++it) {
+        for (int it = 0; found && it < n_iter; ++it) {
             const int s = it % S;
             const uint32_t par = (uint32_t)(it / S) & 1u;
+            // the id of page it + S, which this warp issues if it releases page it last
+            // (read now, used after the page)
+            const int next_id = lane == 0 ? cursor_id() : 0;
             bool ok = mbar_wait(full0 + 8 * s, par, p.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -488,7 +501,18 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            if (lane == 0) {
+                // release the stage; the last warp to do so refills it with page it + S
+                // (the empty barrier's completed phase orders every warp's reads of the
+                // stage before the copy that overwrites it)
+                mbar_arrive(empty0 + 8 * s);
+                if (atomicAdd(&released[s], 1) == Hkv - 1) {
+                    released[s] = 0;
+                    if (cit < n_iter && mbar_wait(empty0 + 8 * s, par, p.status, abort_flag))
+                        issue(next_id);
+                }
+            }
+            advance();
             if (mt.last) {
                 // ---- partial result of this segment -> workspace slot b + cta
                 const long long slot = (long long)cur_b + blockIdx.x;
@@ -534,6 +558,12 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
     }
     __syncwarp();
     __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        // an aborted launch lets the copies it issued land before the CTA exits
+        for (int s = 0; s < S; ++s)
+            if (n_issued[s] > 0)
+                mbar_wait(full0 + 8 * s, (uint32_t)(n_issued[s] - 1) & 1u, p.status, nullptr);
+    }
 }
 
 // One warp per (sequence b, query head h): combine the partial results of the CTAs

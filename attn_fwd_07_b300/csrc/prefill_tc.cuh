@@ -116,7 +116,8 @@ struct PrefillCfg {
     static constexpr int NQ = 4;
     static constexpr int CLAIM = 2;
     static constexpr uint32_t OFF_ITEMS = OFF_STATS + 2 * 128 * 4;
-    static constexpr uint32_t OFF_CTRL = OFF_ITEMS + NQ * 80;
+    // (one more slot holds the item the producer has claimed but not yet published)
+    static constexpr uint32_t OFF_CTRL = OFF_ITEMS + (NQ + 1) * 80;
     static constexpr uint32_t CTRL_BYTES = 512;
     static constexpr size_t SMEM = 1024 + OFF_CTRL + CTRL_BYTES;
     // TMEM columns
@@ -451,7 +452,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
                 // the next item is claimed when this one's last CLAIM key tiles are being
                 // loaded: late enough that the end of the launch evens out, early enough
                 // that its query tiles are in L2 when they are needed
-                PrefillItem nx;
+                PrefillItem &nx = items[C::NQ];  // (kept in shared memory, off the registers)
                 bool have_nx = false;
                 const int j_claim = max(0, it.n_kv - C::CLAIM);
                 const int npg = (it.kvlen + 15) / 16;  // pages holding this sequence's keys
