@@ -298,8 +298,11 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
 
         // A fragments of q (rows 0..7).  FP8 cache: the k-slots of each 16-dim step
         // are permuted so that a lane's K bytes are contiguous -- in half hf, k-step
-        // 4 hf + j takes dims 64 hf + 16 quad + 4 j .. + 3 for this lane's slots
+        // 4 hf + j takes dims 16 (2 quad + hf) + 4 j .. + 3 for this lane's slots
         // (2 quad, 2 quad + 1, 2 quad + 8, 2 quad + 9); q uses the same permutation.
+        // A half's 16-byte chunks are then the even (hf = 0) or the odd ones of a key
+        // row, so the two rows that share a phase of a 16-byte shared load (tokens 2i
+        // and 2i + 1, whose swizzles differ in the lowest bit) fall in distinct banks.
         uint32_t qa[8][2];
         float oacc[16][4];
         // scores are q . k * scale (* the head's key scale for an FP8 cache), log2 units
@@ -308,9 +311,10 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         float m_run = -INFINITY, l_run = 0.f, q_run = 0.f;
         int cur_b = 0;
 
-        for (int it = 0; found && it < n_iter; ++it) {
-            const int s = it % S;
-            const uint32_t par = (uint32_t)(it / S) & 1u;
+        int s = 0;          // ring position (stage, phase parity), advanced by one per page
+        uint32_t par = 0u;
+        for (int it = 0; found && it < n_iter;
+             ++it, s = (s + 1 == S) ? 0 : s + 1, par ^= (s == 0) ? 1u : 0u) {
             // the id of page it + S, which this warp issues if it releases page it last
             // (read now, used after the page)
             const int next_id = lane == 0 ? cursor_id() : 0;
@@ -326,7 +330,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                     if (ks < nk && row_ok) {
                         const uint32_t *qr = reinterpret_cast<const uint32_t *>(qb + row * p.d);
                         if constexpr (FP8) {
-                            const int d0 = (ks >> 2) * 64 + 16 * quad + 4 * (ks & 3);
+                            const int d0 = 32 * quad + 16 * (ks >> 2) + 4 * (ks & 3);
                             qa[ks][0] = bf16x2_to_f16x2(qr[d0 >> 1]);
                             qa[ks][1] = bf16x2_to_f16x2(qr[(d0 + 2) >> 1]);
                         } else {
@@ -360,7 +364,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
                             const uint4 w = lds128(kst + rg * 128u +
-                                                   (uint32_t)(((4 * hf + quad) ^ (int)(rg & 7u)) * 16));
+                                                   (uint32_t)(((2 * quad + hf) ^ (int)(rg & 7u)) * 16));
                             const uint32_t wj[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
@@ -397,11 +401,13 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 sv[1] = sacc[0][1] * sl2;
                 sv[2] = sacc[1][0] * sl2;
                 sv[3] = sacc[1][1] * sl2;
-                const int t0 = 2 * quad;
-                if (t0 >= mt.ntok || t0 < mt.lo) sv[0] = -INFINITY;
-                if (t0 + 1 >= mt.ntok || t0 + 1 < mt.lo) sv[1] = -INFINITY;
-                if (t0 + 8 >= mt.ntok || t0 + 8 < mt.lo) sv[2] = -INFINITY;
-                if (t0 + 9 >= mt.ntok || t0 + 9 < mt.lo) sv[3] = -INFINITY;
+                if (mt.ntok < kDecPage || mt.lo > 0) {  // (a full page needs no mask)
+                    const int t0 = 2 * quad;
+                    if (t0 >= mt.ntok || t0 < mt.lo) sv[0] = -INFINITY;
+                    if (t0 + 1 >= mt.ntok || t0 + 1 < mt.lo) sv[1] = -INFINITY;
+                    if (t0 + 8 >= mt.ntok || t0 + 8 < mt.lo) sv[2] = -INFINITY;
+                    if (t0 + 9 >= mt.ntok || t0 + 9 < mt.lo) sv[3] = -INFINITY;
+                }
                 float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
