@@ -639,6 +639,11 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
+    # The device first spins (about 0.2 ms per timed step) while the host enqueues every
+    # timed step, so that no step's device time includes the host's launch latency: a
+    # small workload's kernel runs shorter than the Python call that launches it.  The
+    # spin lies before the first step's start event.
+    torch.cuda._sleep(int(min(args.steps, 500) * 400_000))
     for s in range(args.steps):
         step(evs[s])
     torch.cuda.synchronize(dev)
