@@ -1,7 +1,7 @@
 // prefill_simt.cuh -- fp32 prefill attention on the CUDA cores (no tensor
 // cores), for fp32 inputs.
 //
-// One CTA owns a tile of 64 query rows of one (sequence, query head) and
+// One CTA owns a tile of 16 query rows of one (sequence, query head) and
 // streams the sequence's keys and values through shared memory 64 at a time,
 // keeping the online-softmax state per row ("Donanıma Duyarlı Algoritma
 // Tasarımı: FlashAttention", section "Online Softmax Prensibi"): a running
@@ -10,18 +10,23 @@
 // Exponentials are taken base 2 with log2(e) folded into the scale; the output
 // is divided by L once at the end and LSE = (M + log2 L) * ln 2.
 //
-// Thread map: 256 threads, four per query row.  Thread (row r, quarter c)
-// computes the scores of keys c, c+4, ... of each 64-key tile, and owns the
-// output columns [c*d/4, (c+1)*d/4) of its row.
+// Thread map: 256 threads, sixteen per query row and sixteen rows per CTA, so that a
+// short sequence still spreads over many SMs (N = 256 is 16 CTAs) and each thread's
+// serial work per key tile stays small.  Thread (row r, lane c16 of its row) computes
+// the scores of keys c16, c16+16, c16+32, c16+48 of each 64-key tile and owns the
+// output columns 4 ch .. 4 ch + 3 of its row for ch = c16 and c16 + 16 (those below
+// d / 4); a row's sixteen threads are one half of a warp, so the row maximum and sum
+// are half-warp shuffles.
 #pragma once
 
 #include "ptx.cuh"
 
 namespace attn07 {
 
-constexpr int kSimtBM = 64;   // query rows per CTA
+constexpr int kSimtBM = 16;   // query rows per CTA
 constexpr int kSimtBN = 64;   // keys per tile
-constexpr int kSimtThreads = 256;
+constexpr int kSimtTPR = 16;  // threads per query row
+constexpr int kSimtThreads = kSimtBM * kSimtTPR;
 constexpr int kSimtMaxD = 128;
 
 struct SimtParams {
@@ -42,10 +47,10 @@ __global__ void __launch_bounds__(kSimtThreads)
 prefill_simt_kernel(const SimtParams p) {
     extern __shared__ __align__(16) float smem_f[];
     const int dp = p.d + 4;  // padded row length (floats)
-    float *Qs = smem_f;                          // [64][dp]
+    float *Qs = smem_f;                          // [16][dp]
     float *Ks = Qs + kSimtBM * dp;               // [64][dp]
     float *Vs = Ks + kSimtBN * dp;               // [64][dp]
-    float *Ps = Vs + kSimtBN * dp;               // [64][68]
+    float *Ps = Vs + kSimtBN * dp;               // [16][68]
 
     const int tile = blockIdx.x;
     const int h = blockIdx.y;
@@ -64,11 +69,10 @@ prefill_simt_kernel(const SimtParams p) {
     if (row0 >= len) return;
 
     const int tid = threadIdx.x;
-    const int r = tid >> 2;     // query row in tile
-    const int c4 = tid & 3;     // quarter
+    const int r = tid / kSimtTPR;   // query row in tile
+    const int c16 = tid % kSimtTPR; // lane within the row
     const int d = p.d;
-    const int dq = d >> 2;      // output columns per thread
-    const int nvec = d >> 2;    // float4 per row
+    const int nvec = d >> 2;        // float4 per row (at most 32: two per thread)
 
     // Q tile, pre-scaled by scale*log2(e) so scores come out in log2 units.
     for (int idx = tid; idx < kSimtBM * nvec; idx += kSimtThreads) {
@@ -84,86 +88,108 @@ prefill_simt_kernel(const SimtParams p) {
     }
 
     float m = -INFINITY, l = 0.f;
-    float acc[kSimtMaxD / 4];
+    float acc[8];  // columns 4 (c16 + 16 i) + e, i < 2, e < 4
 #pragma unroll
-    for (int c = 0; c < kSimtMaxD / 4; ++c) acc[c] = 0.f;
+    for (int c = 0; c < 8; ++c) acc[c] = 0.f;
 
     const int qi = row0 + r;  // this thread's query position
     int kv_end = len;
     if (p.causal) kv_end = min(len, row0 + kSimtBM);
+    constexpr int KPT = kSimtBN / kSimtTPR;  // keys per thread per tile
 
+    // the K and V tiles pass through registers: each thread's share of the next tile
+    // is loaded from device memory while the current one is computed on
+    constexpr int kMaxVec = kSimtBN * kSimtMaxD / 4 / kSimtThreads;  // float4 per thread
+    float4 pk[kMaxVec], pv[kMaxVec];
+    auto fetch = [&](int t0) {
+#pragma unroll
+        for (int i = 0; i < kMaxVec; ++i) {
+            const int idx = tid + kSimtThreads * i;
+            const int rr = idx / nvec, cv = idx % nvec;
+            pk[i] = pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (idx < kSimtBN * nvec && t0 + rr < len) {
+                const int64_t off = ((int64_t)(start + t0 + rr) * p.Hkv + g) * d + cv * 4;
+                pk[i] = *reinterpret_cast<const float4 *>(p.k + off);
+                pv[i] = *reinterpret_cast<const float4 *>(p.v + off);
+            }
+        }
+    };
+    fetch(0);
     for (int kv0 = 0; kv0 < kv_end; kv0 += kSimtBN) {
         __syncthreads();
-        for (int idx = tid; idx < kSimtBN * nvec; idx += kSimtThreads) {
-            const int rr = idx / nvec, cv = idx % nvec;
-            float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-            if (kv0 + rr < len) {
-                const int64_t off = ((int64_t)(start + kv0 + rr) * p.Hkv + g) * d + cv * 4;
-                kk = *reinterpret_cast<const float4 *>(p.k + off);
-                vv = *reinterpret_cast<const float4 *>(p.v + off);
+#pragma unroll
+        for (int i = 0; i < kMaxVec; ++i) {
+            const int idx = tid + kSimtThreads * i;
+            if (idx < kSimtBN * nvec) {
+                const int rr = idx / nvec, cv = idx % nvec;
+                *reinterpret_cast<float4 *>(Ks + rr * dp + cv * 4) = pk[i];
+                *reinterpret_cast<float4 *>(Vs + rr * dp + cv * 4) = pv[i];
             }
-            *reinterpret_cast<float4 *>(Ks + rr * dp + cv * 4) = kk;
-            *reinterpret_cast<float4 *>(Vs + rr * dp + cv * 4) = vv;
         }
         __syncthreads();
+        if (kv0 + kSimtBN < kv_end) fetch(kv0 + kSimtBN);
 
-        // scores of keys c4 + 4*jj
-        float s[kSimtBN / 4];
+        // scores of keys c16 + 16*jj: four independent dot products over d
+        float s[KPT] = {0.f, 0.f, 0.f, 0.f};
+        const float *qr = Qs + r * dp;
+#pragma unroll 4
+        for (int c = 0; c < d; c += 4) {
+            const float4 qa = *reinterpret_cast<const float4 *>(qr + c);
+#pragma unroll
+            for (int jj = 0; jj < KPT; ++jj) {
+                const float4 ka =
+                    *reinterpret_cast<const float4 *>(Ks + (c16 + kSimtTPR * jj) * dp + c);
+                s[jj] = fmaf(qa.x, ka.x, s[jj]);
+                s[jj] = fmaf(qa.y, ka.y, s[jj]);
+                s[jj] = fmaf(qa.z, ka.z, s[jj]);
+                s[jj] = fmaf(qa.w, ka.w, s[jj]);
+            }
+        }
         float tmax = -INFINITY;
 #pragma unroll
-        for (int jj = 0; jj < kSimtBN / 4; ++jj) {
-            const int j = c4 + 4 * jj;
-            const float *qr = Qs + r * dp;
-            const float *kr = Ks + j * dp;
-            float a = 0.f;
-            for (int c = 0; c < d; c += 4) {
-                const float4 qa = *reinterpret_cast<const float4 *>(qr + c);
-                const float4 ka = *reinterpret_cast<const float4 *>(kr + c);
-                a = fmaf(qa.x, ka.x, a);
-                a = fmaf(qa.y, ka.y, a);
-                a = fmaf(qa.z, ka.z, a);
-                a = fmaf(qa.w, ka.w, a);
-            }
-            const int kj = kv0 + j;
+        for (int jj = 0; jj < KPT; ++jj) {
+            const int kj = kv0 + c16 + kSimtTPR * jj;
             const bool ok = kj < len && (!p.causal || kj <= qi);
-            s[jj] = ok ? a : -INFINITY;
+            s[jj] = ok ? s[jj] : -INFINITY;
             tmax = fmaxf(tmax, s[jj]);
         }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+#pragma unroll
+        for (int o = kSimtTPR / 2; o > 0; o >>= 1)
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
         const float m_new = fmaxf(m, tmax);
         // a row with no allowed key yet keeps m = -inf; shift by 0 then
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = ex2(m - m_use);
         float tsum = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < kSimtBN / 4; ++jj) {
+        for (int jj = 0; jj < KPT; ++jj) {
             const float pj = ex2(s[jj] - m_use);
             tsum += pj;
-            Ps[r * (kSimtBN + 4) + c4 + 4 * jj] = pj;
+            Ps[r * (kSimtBN + 4) + c16 + kSimtTPR * jj] = pj;
         }
-        tsum += __shfl_xor_sync(0xffffffffu, tsum, 1);
-        tsum += __shfl_xor_sync(0xffffffffu, tsum, 2);
+#pragma unroll
+        for (int o = kSimtTPR / 2; o > 0; o >>= 1)
+            tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
         l = l * alpha + tsum;
         m = m_new;
-        __syncwarp();
+        __syncwarp();  // (a row's P is written and read by its own half-warp)
         // O = O * alpha + P V over this thread's columns
-        const int cbase = c4 * dq;
 #pragma unroll
-        for (int c = 0; c < kSimtMaxD / 4; ++c)
-            if (c < dq) acc[c] *= alpha;
+        for (int c = 0; c < 8; ++c) acc[c] *= alpha;
         const int jmax = min(kSimtBN, kv_end - kv0);
+#pragma unroll 4
         for (int j = 0; j < jmax; ++j) {
             const float pj = Ps[r * (kSimtBN + 4) + j];
-            const float *vr = Vs + j * dp + cbase;
+            const float *vr = Vs + j * dp;
 #pragma unroll
-            for (int c = 0; c < kSimtMaxD / 4; c += 4) {
-                if (c < dq) {
-                    const float4 va = *reinterpret_cast<const float4 *>(vr + c);
-                    acc[c] = fmaf(pj, va.x, acc[c]);
-                    acc[c + 1] = fmaf(pj, va.y, acc[c + 1]);
-                    acc[c + 2] = fmaf(pj, va.z, acc[c + 2]);
-                    acc[c + 3] = fmaf(pj, va.w, acc[c + 3]);
+            for (int i = 0; i < 2; ++i) {
+                const int ch = c16 + kSimtTPR * i;
+                if (ch < nvec) {
+                    const float4 va = *reinterpret_cast<const float4 *>(vr + 4 * ch);
+                    acc[4 * i] = fmaf(pj, va.x, acc[4 * i]);
+                    acc[4 * i + 1] = fmaf(pj, va.y, acc[4 * i + 1]);
+                    acc[4 * i + 2] = fmaf(pj, va.z, acc[4 * i + 2]);
+                    acc[4 * i + 3] = fmaf(pj, va.w, acc[4 * i + 3]);
                 }
             }
         }
@@ -171,15 +197,17 @@ prefill_simt_kernel(const SimtParams p) {
 
     if (qi < len) {
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        float *orow = p.o + ((int64_t)(start + qi) * p.Hq + h) * d + c4 * dq;
+        float *orow = p.o + ((int64_t)(start + qi) * p.Hq + h) * d;
 #pragma unroll
-        for (int c = 0; c < kSimtMaxD / 4; c += 4) {
-            if (c < dq) {
-                *reinterpret_cast<float4 *>(orow + c) =
-                    make_float4(acc[c] * inv, acc[c + 1] * inv, acc[c + 2] * inv, acc[c + 3] * inv);
+        for (int i = 0; i < 2; ++i) {
+            const int ch = c16 + kSimtTPR * i;
+            if (ch < nvec) {
+                *reinterpret_cast<float4 *>(orow + 4 * ch) =
+                    make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv,
+                                acc[4 * i + 3] * inv);
             }
         }
-        if (p.lse && c4 == 0) {
+        if (p.lse && c16 == 0) {
             const float lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
             int64_t idx;
             if (p.cu_seqlens) idx = (int64_t)h * p.total + start + qi;

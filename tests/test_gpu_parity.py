@@ -136,6 +136,10 @@ def test_prefill_maximum_jumps_inside_a_key_tile(oracle, keys, Hq, Hkv):
 @pytest.mark.parametrize("B,N,Hq,Hkv,d,causal", [
     (1, 1, 1, 1, 64, False), (1, 63, 2, 1, 64, True), (1, 65, 1, 1, 128, False),
     (2, 129, 4, 2, 64, True), (1, 255, 2, 2, 32, False), (1, 300, 4, 1, 128, True),
+    # every head dimension the kernel takes: a row's sixteen threads own d / 4 float4
+    # column groups between them, one or two each, some none
+    (1, 70, 2, 1, 16, True), (1, 100, 1, 1, 48, False), (2, 90, 2, 2, 80, True),
+    (1, 130, 3, 1, 96, False), (1, 77, 2, 2, 112, True),
 ])
 def test_prefill_f32_small(oracle, B, N, Hq, Hkv, d, causal):
     w = inputs.dense(B, N, Hq, Hkv, d, 2000 + N + d, torch.float32, causal=causal)
