@@ -18,18 +18,20 @@
 // two tiles' softmax runs while the tensor core works on the other tile
 // ("ping-pong").
 //
-// Persistent CTAs: one CTA per SM.  Its producer warp takes item indices in order
-// (heaviest first) from the launch's work counter whenever it is ready for the
-// next one (the first is the CTA's own index), decodes each item once, skips those with nothing to compute, and hands
-// the decoded items to the other roles through a small queue in shared memory.
-// Each role keeps its own ring positions and barrier phases across items, so the
-// next item's query tiles and first key tiles load, and its first products run,
-// while the previous item's output is still being written.
+// Persistent CTAs: one CTA per SM.  CTA c starts on item c; its producer warp
+// takes the next item index (heaviest first) from the launch's work counter while
+// it loads the current item's last two key tiles, decodes each item once, skips
+// blocks of items with nothing to compute, and hands the decoded items to the other
+// roles through a small queue in shared memory.  Each role keeps its own ring
+// positions and barrier phases across items, so the next item's query tiles and
+// first key tiles load, and its first products run, while the previous item's
+// output is still being written.
 //
 // Warp roles (512 threads, four warpgroups):
 //   warps 0-3    softmax of tile 0, one thread per query row (TMEM lane)
 //   warps 4-7    softmax of tile 1
-//   warps 8-11   epilogue: O / L -> bf16 rows in device memory, for both tiles
+//   warps 8-11   epilogue: O / L -> bf16 rows in device memory (32-byte stores),
+//                for both tiles
 //   warp 12      TMA producer: both Q tiles of an item, then K_j / V_j (128
 //                keys) into two shared-memory rings (128-byte swizzle)
 //   warp 13      MMA issuer (one thread), in this order for every j (PV with
