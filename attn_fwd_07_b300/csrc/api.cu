@@ -29,8 +29,8 @@ __device__ unsigned int g_attn_status;
 // Work counters of the tensor-core prefill, two per slot (next item, CTAs done).  A
 // launch takes the next slot in turn; it leaves its counters at zero when its last CTA
 // ends, so a slot is ready for reuse (a replayed graph reuses its launches' slots).
-// Launches in flight at the same time, on other streams, use other slots, up to 64.
-constexpr int kWorkSlots = 64;
+// Launches in flight at the same time, on other streams, use other slots, up to 1024.
+constexpr int kWorkSlots = 1024;
 __device__ unsigned g_prefill_work[2 * kWorkSlots];
 
 namespace {

@@ -31,7 +31,11 @@
  *     are written.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) and runs asynchronously; the return value reports argument
- *     validation and launch errors only.
+ *     validation and launch errors only.  Calls may run concurrently on
+ *     different streams.  The tensor-core prefill takes its work items from a
+ *     counter in a library-owned device array of 1024 slots, one per launch in
+ *     turn, which each launch leaves at zero when it ends: a launch must end
+ *     before the 1024th prefill launch after it in the same process starts.
  *   - Invalid arguments return ATTN_ERR_INVALID_ARG and launch nothing;
  *     sizes outside what the kernels implement return ATTN_ERR_UNSUPPORTED and
  *     launch nothing.  Launch failures return ATTN_ERR_CUDA.

@@ -1,15 +1,16 @@
 """The tensor-core prefill's work scheduling (GPU).
 
 The persistent CTAs take their work items from a counter in device memory, one of
-64 slots taken in turn by the library's launches; the last CTA of a launch sets its
+1024 slots taken in turn by the library's launches; the last CTA of a launch sets its
 counter back to zero.  Items are (query-tile level, sequence, head pair) blocks; a
 block past a packed sequence's end has no work, and the producer that meets one
 moves the counter past the following blocks without work in one step.  None of this
 may change a result, so these tests compare against the fp64 oracle or against a
 launch whose result is already checked:
 
-- many launches in flight on several streams at once (every slot in use, several
-  times over) give bitwise the result of one launch on its own;
+- many launches in flight on several streams at once give bitwise the result of one
+  launch on its own, also after more launches than there are slots (every slot
+  reused);
 - packed batches where most blocks have no work (one long sequence among many
   short ones, sequences past the counter's first scan of 64 blocks) match the
   oracle, and so does a batch where every block of the top levels is empty.
@@ -54,6 +55,24 @@ def test_launches_on_many_streams_match_one_launch():
     torch.cuda.synchronize()
     assert A.attn_get_device_status() == 0
     for o, lse in outs:
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+def test_more_launches_than_counter_slots():
+    w = inputs.dense(1, 300, 4, 2, 128, 5502)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    o_ref, lse_ref = A.attn_fwd(q, k, v, True, w.scale)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    bufs = [(torch.empty_like(q), torch.empty_like(lse_ref)) for _ in streams]
+    for i in range(1100):                      # past the 1024 slots
+        st = streams[i % len(streams)]
+        o, lse = bufs[i % len(streams)]
+        with torch.cuda.stream(st):
+            A.attn_fwd(q, k, v, True, w.scale, o=o, lse=lse, stream=st)
+    torch.cuda.synchronize()
+    assert A.attn_get_device_status() == 0
+    for o, lse in bufs:
         assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
 
 
