@@ -44,7 +44,8 @@
 //                and a commit after S_{j+1} also covers that PV product.
 //   warps 14-15  idle (they complete the fourth warpgroup)
 // The softmax warpgroups raise their register count to 184 per thread; the
-// other two lower theirs to 72 (184 + 72 = twice the 128 of the launch).
+// epilogue warpgroup lowers its to 64 and the producer / MMA warpgroup to 80
+// (2 x 184 + 64 + 80 = four times the 128 of the launch).
 //
 // Softmax step for tile t and key tile j (thread = row): load the S row from
 // TMEM, mask (causal diagonal / window / sequence end), running maximum, P =
@@ -125,15 +126,17 @@ struct PrefillCfg {
     // TMEM columns
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 384;
     static constexpr int THREADS = 512;
-    // per-thread registers after the split: softmax warpgroups / the other two, and the
-    // registers the split needs in all (at most what the launch reserves)
-    static constexpr uint32_t REG_SOFTMAX = 184, REG_OTHER = 72;
-    static constexpr uint32_t REG_NEED = 128 * (2 * REG_SOFTMAX + 2 * REG_OTHER);
+    // per-thread registers after the split: softmax warpgroups, epilogue warpgroup, the
+    // producer / MMA warpgroup; and the registers the split needs in all (at most what
+    // the launch reserves)
+    static constexpr uint32_t REG_SOFTMAX = 184, REG_EPI = 64, REG_OTHER = 80;
+    static constexpr uint32_t REG_NEED = 128 * (2 * REG_SOFTMAX + REG_EPI + REG_OTHER);
 };
 
 static_assert(PrefillCfg<128>::SMEM <= 227 * 1024, "prefill shared memory");
 // four warpgroups of 128 threads share the 65536 registers the launch reserves
-static_assert(128 * (2 * PrefillCfg<128>::REG_SOFTMAX + 2 * PrefillCfg<128>::REG_OTHER) == 65536,
+static_assert(128 * (2 * PrefillCfg<128>::REG_SOFTMAX + PrefillCfg<128>::REG_EPI +
+                     PrefillCfg<128>::REG_OTHER) == 65536,
               "register split must add up to the launch's registers");
 
 // barrier slots inside the control block (8 bytes each)
@@ -972,7 +975,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmQ
         }
     } else {
         // ============================ epilogue: thread = query row of both tiles
-        setmaxnreg_dec<C::REG_OTHER>();
+        setmaxnreg_dec<C::REG_EPI>();
         {
             const int r = threadIdx.x & 127;       // row in tile = TMEM lane
             const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
