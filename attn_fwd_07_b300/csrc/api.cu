@@ -130,7 +130,10 @@ attn_status_t device_state(DeviceState **out) {
         st.work = static_cast<unsigned *>(sym);
         if ((e = cudaFuncSetAttribute(prefill_simt_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)prefill_simt_smem_bytes(kSimtMaxD))) != cudaSuccess)
+                                      (int)prefill_simt_smem_bytes(kSimtMaxD))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prefill_simt_rows4_kernel,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)prefill_simt_rows4_smem_bytes(kSimtMaxD))) != cudaSuccess)
             return cuda_fail(e);
         if ((e = prefill_attrs<128>()) != cudaSuccess || (e = prefill_attrs<64>()) != cudaSuccess)
             return cuda_fail(e);
@@ -390,13 +393,21 @@ attn_status_t attn_fwd_chunked_paged(const void *q, const void *k_cache, const v
                              reinterpret_cast<cudaStream_t>(stream), &pk);
 }
 
-attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+namespace {
+
+// fp32 prefill with `rows` query rows per CTA: 16 (prefill_simt_kernel) or 4
+// (prefill_simt_rows4_kernel); 0 lets the launch size decide: 4-row CTAs when the
+// 16-row grid would fill at most half of the SMs (each SM then gets one or two
+// 4-row CTAs instead of leaving most SMs idle), 16-row CTAs otherwise (each K/V
+// tile loaded into shared memory then serves 16 rows).
+attn_status_t fwd_f32_impl(const float *q, const float *k, const float *v, float *o, float *lse,
                            int B, int Hq, int Hkv, int N, int d, int causal, float scale,
-                           attn_stream_t stream) {
+                           int rows, attn_stream_t stream) {
     if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (rows != 0 && rows != kSimtBM && rows != kSimt4BM) return ATTN_ERR_INVALID_ARG;
     if (d > kSimtMaxD || d % 16 != 0) return ATTN_ERR_UNSUPPORTED;
     if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
     DeviceState *st = nullptr;
@@ -416,10 +427,35 @@ attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float
     p.d = d;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = scale * kLog2e;
-    dim3 grid((N + kSimtBM - 1) / kSimtBM, Hq, B);
-    prefill_simt_kernel<<<grid, kSimtThreads, prefill_simt_smem_bytes(d),
-                          reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    if (rows == 0) {
+        const long long ctas16 = (long long)((N + kSimtBM - 1) / kSimtBM) * Hq * B;
+        rows = 2 * ctas16 <= st->sms ? kSimt4BM : kSimtBM;
+    }
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (rows == kSimt4BM) {
+        dim3 grid((N + kSimt4BM - 1) / kSimt4BM, Hq, B);
+        prefill_simt_rows4_kernel<<<grid, kSimtThreads, prefill_simt_rows4_smem_bytes(d), cs>>>(p);
+    } else {
+        dim3 grid((N + kSimtBM - 1) / kSimtBM, Hq, B);
+        prefill_simt_kernel<<<grid, kSimtThreads, prefill_simt_smem_bytes(d), cs>>>(p);
+    }
     return launch_status();
+}
+
+}  // namespace
+
+attn_status_t attn_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+                           int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                           attn_stream_t stream) {
+    return fwd_f32_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, 0, stream);
+}
+
+attn_status_t attn_testing_fwd_f32_rows(const float *q, const float *k, const float *v, float *o,
+                                        float *lse, int B, int Hq, int Hkv, int N, int d,
+                                        int causal, float scale, int rows,
+                                        attn_stream_t stream) {
+    if (rows != kSimtBM && rows != kSimt4BM) return ATTN_ERR_INVALID_ARG;
+    return fwd_f32_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, rows, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int d, int max_pages_per_seq, int page_size) {

@@ -1,33 +1,38 @@
 // prefill_simt.cuh -- fp32 prefill attention on the CUDA cores (no tensor
 // cores), for fp32 inputs.
 //
-// One CTA owns a tile of 16 query rows of one (sequence, query head) and
-// streams the sequence's keys and values through shared memory 64 at a time,
-// keeping the online-softmax state per row ("Donanıma Duyarlı Algoritma
-// Tasarımı: FlashAttention", section "Online Softmax Prensibi"): a running
-// maximum M and sum L, and the output rescaled by exp(M_old - M_new) whenever
-// the maximum grows, so that no score row is ever written to device memory.
-// Exponentials are taken base 2 with log2(e) folded into the scale; the output
-// is divided by L once at the end and LSE = (M + log2 L) * ln 2.
+// A CTA owns a tile of query rows of one (sequence, query head) and streams the
+// sequence's keys and values through shared memory 64 at a time, keeping the
+// online-softmax state per row ("Donanıma Duyarlı Algoritma Tasarımı:
+// FlashAttention", section "Online Softmax Prensibi"): a running maximum M and
+// sum L, and the output rescaled by exp(M_old - M_new) whenever the maximum
+// grows, so that no score row is ever written to device memory.  Exponentials
+// are taken base 2 with log2(e) folded into the scale; the output is divided by
+// L once at the end and LSE = (M + log2 L) * ln 2.
 //
-// Thread map: 256 threads, sixteen per query row and sixteen rows per CTA, so that a
-// short sequence still spreads over many SMs (N = 256 is 16 CTAs) and each thread's
-// serial work per key tile stays small.  Thread (row r, lane c16 of its row) computes
-// the scores of keys c16, c16+16, c16+32, c16+48 of each 64-key tile and owns the
-// output columns 4 ch .. 4 ch + 3 of its row for ch = c16 and c16 + 16 (those below
-// d / 4); a row's sixteen threads are one half of a warp, so the row maximum and sum
-// are half-warp shuffles.
+// Two thread maps, the tile height chosen per launch (the page's item on block
+// sizes chosen per hardware and sequence length, section "FlashAttention-2:
+// Optimizasyonlar ve İyileştirmeler"):
+// - prefill_simt_kernel: 16 rows per CTA, 16 threads per row.  Each K/V tile
+//   loaded into shared memory serves 16 rows: the choice when the launch has
+//   enough CTAs to fill the GPU.
+// - prefill_simt_rows4_kernel: 4 rows per CTA, 64 threads per row, for launches
+//   that would leave most SMs idle with 16-row tiles (N = 256 on one head is 16
+//   such CTAs, or 64 of 4 rows).
 #pragma once
 
 #include "ptx.cuh"
 
 namespace attn07 {
 
-constexpr int kSimtBM = 16;   // query rows per CTA
+constexpr int kSimtBM = 16;   // query rows per CTA (prefill_simt_kernel)
 constexpr int kSimtBN = 64;   // keys per tile
-constexpr int kSimtTPR = 16;  // threads per query row
+constexpr int kSimtTPR = 16;  // threads per query row (prefill_simt_kernel)
+constexpr int kSimt4BM = 4;   // query rows per CTA (prefill_simt_rows4_kernel)
+constexpr int kSimt4TPR = 64; // threads per query row (prefill_simt_rows4_kernel)
 constexpr int kSimtThreads = kSimtBM * kSimtTPR;
 constexpr int kSimtMaxD = 128;
+static_assert(kSimt4BM * kSimt4TPR == kSimtThreads, "both thread maps use 256 threads");
 
 struct SimtParams {
     const float *q;
@@ -43,6 +48,11 @@ struct SimtParams {
     float scale_log2;           // scale * log2(e)
 };
 
+// 16 rows per CTA, 256 threads, sixteen per query row.  Thread (row r, lane
+// c16 of its row) computes the scores of keys c16, c16+16, c16+32, c16+48 of each
+// 64-key tile and owns the output columns 4 ch .. 4 ch + 3 of its row for ch = c16
+// and c16 + 16 (those below d / 4); a row's sixteen threads are one half of a warp,
+// so the row maximum and sum are half-warp shuffles.
 __global__ void __launch_bounds__(kSimtThreads)
 prefill_simt_kernel(const SimtParams p) {
     extern __shared__ __align__(16) float smem_f[];
@@ -219,6 +229,206 @@ prefill_simt_kernel(const SimtParams p) {
 
 inline size_t prefill_simt_smem_bytes(int d) {
     return sizeof(float) * ((size_t)(kSimtBM + 2 * kSimtBN) * (d + 4) + kSimtBM * (kSimtBN + 4));
+}
+
+// 4 rows per CTA, 256 threads, 64 per query row (two warps).  Thread (row r, lane c
+// of its row):
+// - scores: key c of each 64-key tile, one dot product over d with the row's Q (a
+//   warp-wide broadcast) and key row c (32 rows per warp, conflict-free with the
+//   padded row length);
+// - output: columns c and c + 64 of its row (those below d), so that a warp's value
+//   loads are 32 consecutive words of one value row.
+// The row maximum and sum are warp shuffles, then one exchange between the row's two
+// warps through shared memory.  (One CTA per SM: the registers hold a K/V tile's
+// share and its slots' offsets.)
+__global__ void __launch_bounds__(kSimtThreads, 1)
+prefill_simt_rows4_kernel(const SimtParams p) {
+    extern __shared__ __align__(16) float smem_f[];
+    const int dp = p.d + 4;  // padded row length (floats)
+    float *Qs = smem_f;                          // [4][dp]
+    float *Ks = Qs + kSimt4BM * dp;              // [64][dp]
+    float *Vs = Ks + kSimtBN * dp;               // [64][dp]
+    float *Ps = Vs + kSimtBN * dp;               // [4][64]
+    float *red = Ps + kSimt4BM * kSimtBN;        // [2][4][2]: row maxima, row sums per warp
+
+    const int tile = blockIdx.x;
+    const int h = blockIdx.y;
+    const int seq = blockIdx.z;
+    const int g = h / (p.Hq / p.Hkv);
+
+    int start, len;
+    if (p.cu_seqlens) {
+        start = p.cu_seqlens[seq];
+        len = p.cu_seqlens[seq + 1] - start;
+    } else {
+        start = seq * p.N;
+        len = p.N;
+    }
+    const int row0 = tile * kSimt4BM;
+    if (row0 >= len) return;
+
+    const int tid = threadIdx.x;
+    const int r = tid / kSimt4TPR;   // query row in tile
+    const int c = tid % kSimt4TPR;   // lane within the row: key c, output columns c, c + 64
+    const int half = c >> 5;         // the row's warp
+    const int lane = tid & 31;
+    const int d = p.d;
+    const int nvec = d >> 2;         // float4 per row
+
+    // Q tile, pre-scaled by scale*log2(e) so scores come out in log2 units.
+    for (int idx = tid; idx < kSimt4BM * nvec; idx += kSimtThreads) {
+        const int rr = idx / nvec, cv = idx % nvec;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row0 + rr < len) {
+            val = *reinterpret_cast<const float4 *>(
+                p.q + ((int64_t)(start + row0 + rr) * p.Hq + h) * d + cv * 4);
+            val.x *= p.scale_log2; val.y *= p.scale_log2;
+            val.z *= p.scale_log2; val.w *= p.scale_log2;
+        }
+        *reinterpret_cast<float4 *>(Qs + rr * dp + cv * 4) = val;
+    }
+
+    float m = -INFINITY, l = 0.f;
+    float acc0 = 0.f, acc1 = 0.f;  // output columns c and c + 64
+
+    const int qi = row0 + r;  // this thread's query position
+    int kv_end = len;
+    if (p.causal) kv_end = min(len, row0 + kSimt4BM);
+
+    // the K and V tiles pass through registers: each thread's share of the next tile
+    // is loaded from device memory while the current one is computed on (rows past
+    // the sequence are zeros).  A thread's share is the same float4 slots of every
+    // tile: their rows, shared-memory offsets and device offsets (relative to the
+    // tile's first row) are computed once.
+    constexpr int kMaxVec = kSimtBN * kSimtMaxD / 4 / kSimtThreads;  // float4 per thread
+    float4 pk[kMaxVec], pv[kMaxVec];
+    int vrow[kMaxVec], soff[kMaxVec], goff[kMaxVec];
+#pragma unroll
+    for (int i = 0; i < kMaxVec; ++i) {
+        const int idx = tid + kSimtThreads * i;
+        vrow[i] = kSimtBN;  // (no slot)
+        soff[i] = goff[i] = 0;
+        if (idx < kSimtBN * nvec) {
+            const int rr = idx / nvec, cv = idx - rr * nvec;
+            vrow[i] = rr;
+            soff[i] = rr * dp + cv * 4;
+            goff[i] = rr * p.Hkv * d + cv * 4;
+        }
+    }
+    auto fetch = [&](int t0) {
+        const int lim = min(kSimtBN, len - t0);
+        const int64_t base = ((int64_t)(start + t0) * p.Hkv + g) * d;
+#pragma unroll
+        for (int i = 0; i < kMaxVec; ++i) {
+            pk[i] = pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (vrow[i] < lim) {
+                pk[i] = *reinterpret_cast<const float4 *>(p.k + base + goff[i]);
+                pv[i] = *reinterpret_cast<const float4 *>(p.v + base + goff[i]);
+            }
+        }
+    };
+    fetch(0);
+    for (int kv0 = 0; kv0 < kv_end; kv0 += kSimtBN) {
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kMaxVec; ++i) {
+            if (vrow[i] < kSimtBN) {
+                *reinterpret_cast<float4 *>(Ks + soff[i]) = pk[i];
+                *reinterpret_cast<float4 *>(Vs + soff[i]) = pv[i];
+            }
+        }
+        __syncthreads();
+        if (kv0 + kSimtBN < kv_end) fetch(kv0 + kSimtBN);
+
+        // score of key c: four partial sums over d (one per float4 component)
+        const float *qr = Qs + r * dp;
+        const float *kr = Ks + c * dp;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+        for (int cc = 0; cc < d; cc += 4) {
+            const float4 qa = *reinterpret_cast<const float4 *>(qr + cc);
+            const float4 ka = *reinterpret_cast<const float4 *>(kr + cc);
+            a0 = fmaf(qa.x, ka.x, a0);
+            a1 = fmaf(qa.y, ka.y, a1);
+            a2 = fmaf(qa.z, ka.z, a2);
+            a3 = fmaf(qa.w, ka.w, a3);
+        }
+        const int kj = kv0 + c;
+        const bool ok = kj < len && (!p.causal || kj <= qi);
+        const float s = ok ? (a0 + a1) + (a2 + a3) : -INFINITY;
+
+        // row maximum: the warp's, then the row's two warps' through shared memory
+        float tmax = s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+        if (lane == 0) red[r * 2 + half] = tmax;
+        __syncthreads();
+        tmax = fmaxf(red[r * 2], red[r * 2 + 1]);
+        const float m_new = fmaxf(m, tmax);
+        // a row with no allowed key yet keeps m = -inf; shift by 0 then
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2(m - m_use);
+        const float pj = ex2(s - m_use);  // 0 for a masked key
+        Ps[r * kSimtBN + c] = pj;
+        float tsum = pj;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
+        if (lane == 0) red[8 + r * 2 + half] = tsum;
+        __syncthreads();
+        l = l * alpha + (red[8 + r * 2] + red[8 + r * 2 + 1]);
+        m = m_new;
+
+        // O = O * alpha + P V over this thread's columns.  Keys from the tile's end up
+        // to the next multiple of 4 have P = 0 and finite (or zero-filled) values.
+        acc0 *= alpha;
+        acc1 *= alpha;
+        const int jmax = (min(kSimtBN, kv_end - kv0) + 3) & ~3;
+        const float *pr = Ps + r * kSimtBN;
+        if (c + 64 < d) {
+#pragma unroll 2
+            for (int j = 0; j < jmax; j += 4) {
+                const float4 p4 = *reinterpret_cast<const float4 *>(pr + j);
+                const float *vr = Vs + j * dp + c;
+                acc0 = fmaf(p4.x, vr[0], acc0);
+                acc1 = fmaf(p4.x, vr[64], acc1);
+                acc0 = fmaf(p4.y, vr[dp], acc0);
+                acc1 = fmaf(p4.y, vr[dp + 64], acc1);
+                acc0 = fmaf(p4.z, vr[2 * dp], acc0);
+                acc1 = fmaf(p4.z, vr[2 * dp + 64], acc1);
+                acc0 = fmaf(p4.w, vr[3 * dp], acc0);
+                acc1 = fmaf(p4.w, vr[3 * dp + 64], acc1);
+            }
+        } else if (c < d) {
+#pragma unroll 2
+            for (int j = 0; j < jmax; j += 4) {
+                const float4 p4 = *reinterpret_cast<const float4 *>(pr + j);
+                const float *vr = Vs + j * dp + c;
+                acc0 = fmaf(p4.x, vr[0], acc0);
+                acc0 = fmaf(p4.y, vr[dp], acc0);
+                acc0 = fmaf(p4.z, vr[2 * dp], acc0);
+                acc0 = fmaf(p4.w, vr[3 * dp], acc0);
+            }
+        }
+    }
+
+    if (qi < len) {
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+        float *orow = p.o + ((int64_t)(start + qi) * p.Hq + h) * d;
+        if (c < d) orow[c] = acc0 * inv;
+        if (c + 64 < d) orow[c + 64] = acc1 * inv;
+        if (p.lse && c == 0) {
+            const float lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            int64_t idx;
+            if (p.cu_seqlens) idx = (int64_t)h * p.total + start + qi;
+            else idx = ((int64_t)seq * p.Hq + h) * p.N + qi;
+            p.lse[idx] = lse;
+        }
+    }
+}
+
+inline size_t prefill_simt_rows4_smem_bytes(int d) {
+    return sizeof(float) *
+           ((size_t)(kSimt4BM + 2 * kSimtBN) * (d + 4) + kSimt4BM * kSimtBN + 16);
 }
 
 }  // namespace attn07

@@ -165,6 +165,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "prefill_tc_kernel": ("prefill_tc.cuh", "ptx.cuh"),
     "prefill_simt_kernel": ("prefill_simt.cuh", "ptx.cuh"),
+    "prefill_simt_rows4_kernel": ("prefill_simt.cuh", "ptx.cuh"),
     "decode_split_kernel": ("decode.cuh", "ptx.cuh"),
     "decode_split_kernel<true>": ("decode.cuh", "ptx.cuh"),
 }
@@ -335,7 +336,7 @@ class Leg:
             self.f32 = w.q.dtype == torch.float32
             self.work, self.unit = prefill_flops(w), "TFLOP/s"
             self.bound = "alu" if self.f32 else "tensor"
-            self.kernel = "prefill_simt_kernel" if self.f32 else "prefill_tc_kernel"
+            self.kernel = simt_kernel(w.q.shape, dev) if self.f32 else "prefill_tc_kernel"
         self.shape = workload_shape(self.kind, w, self.spec)
         # end to end: a decode step's query, page table and lengths come from the host and
         # its O and LSE go back, while the cache stays resident on the device (where a
@@ -403,6 +404,15 @@ class Leg:
         del self.h_in, self.h_out
         if self.kind == "dense" and not self.f32:
             self.A.attn_release_host_staging()
+
+
+def simt_kernel(q_shape, dev) -> str:
+    """The fp32 kernel attn_fwd_f32 launches for q of shape [B, N, Hq, d]: 4-row CTAs
+    when 16-row CTAs would fill at most half of the SMs, else 16-row CTAs."""
+    B, N, Hq, _ = q_shape
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return ("prefill_simt_rows4_kernel" if 2 * ((N + 15) // 16) * Hq * B <= sms
+            else "prefill_simt_kernel")
 
 
 def launches_per_call(leg) -> int:

@@ -31,6 +31,21 @@ attn_status_t attn_testing_decode_paged_ctas(const void *q, const void *k_cache,
                                              size_t workspace_bytes, int ctas,
                                              attn_stream_t stream);
 
+/*
+ * attn_fwd_f32 with a fixed tile height: `rows` = 16 (16 query rows per CTA,
+ * 16 threads per row) or 4 (4 rows per CTA, 64 threads per row) instead of the
+ * library's choice by launch size.  Both compute the same attention formula
+ * (the fatihsoysal.com page, section "Transformer Mimarisi ve Self-Attention
+ * Mekanizması") with the online softmax of section "Online Softmax Prensibi",
+ * in fp32; their results differ only by the order of fp32 additions.
+ * Arguments, layouts and errors as attn_fwd_f32; any other `rows` returns
+ * ATTN_ERR_INVALID_ARG.
+ */
+attn_status_t attn_testing_fwd_f32_rows(const float *q, const float *k, const float *v, float *o,
+                                        float *lse, int B, int Hq, int Hkv, int N, int d,
+                                        int causal, float scale, int rows,
+                                        attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

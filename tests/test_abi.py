@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_test_hooks_stay_out_of_the_interface():
     hooks = declared_functions(TEST_HEADER)
-    assert hooks == ["attn_testing_decode_paged_ctas"]
+    assert hooks == ["attn_testing_decode_paged_ctas", "attn_testing_fwd_f32_rows"]
     assert not set(hooks) & set(declared_functions())
 
 
@@ -114,6 +114,20 @@ def test_f32_head_dim_rule(lib):
                                 None) == A.ATTN_ERR_UNSUPPORTED, d
     text = open(HEADER).read()
     assert "16 <= d <= 128 and d % 16 == 0" in text
+
+
+def test_f32_rows_hook_takes_the_two_tile_heights(lib):
+    """attn_testing_fwd_f32_rows runs 16-row or 4-row CTAs; any other height is refused
+    before anything is launched, and the shared argument rules still apply."""
+    P = ctypes.c_void_p
+    p = P(1 << 20)
+    fn = lib.attn_testing_fwd_f32_rows
+    fn.argtypes = [P, P, P, P, P] + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, P]
+    fn.restype = ctypes.c_int
+    for rows in (0, 1, 8, 32, -4):
+        assert fn(p, p, p, p, None, 1, 1, 1, 8, 64, 1, 0.1, rows, None) == A.ATTN_ERR_INVALID_ARG
+    assert fn(None, p, p, p, None, 1, 1, 1, 8, 64, 1, 0.1, 4, None) == A.ATTN_ERR_INVALID_ARG
+    assert fn(p, p, p, p, None, 1, 1, 1, 8, 24, 1, 0.1, 16, None) == A.ATTN_ERR_UNSUPPORTED
 
 
 def test_workspace_size_signature():

@@ -3,6 +3,7 @@ same seeded inputs, element by element, at sizes that span several tiles and a
 ragged tail, at the five workloads' full sizes (sampled rows where the oracle
 would take minutes), and on edge cases.  Tolerances are in tests/parity.py.
 """
+import ctypes
 import math
 
 import numpy as np
@@ -136,10 +137,14 @@ def test_prefill_maximum_jumps_inside_a_key_tile(oracle, keys, Hq, Hkv):
 @pytest.mark.parametrize("B,N,Hq,Hkv,d,causal", [
     (1, 1, 1, 1, 64, False), (1, 63, 2, 1, 64, True), (1, 65, 1, 1, 128, False),
     (2, 129, 4, 2, 64, True), (1, 255, 2, 2, 32, False), (1, 300, 4, 1, 128, True),
-    # every head dimension the kernel takes: a row's sixteen threads own d / 4 float4
-    # column groups between them, one or two each, some none
+    # every head dimension the kernel takes: a row's 64 threads own output columns c and
+    # c + 64 below d, two, one or none each
     (1, 70, 2, 1, 16, True), (1, 100, 1, 1, 48, False), (2, 90, 2, 2, 80, True),
     (1, 130, 3, 1, 96, False), (1, 77, 2, 2, 112, True),
+    # CTAs of 4 query rows: sequences shorter than one, ragged last CTAs, and many key
+    # tiles below the causal diagonal
+    (1, 2, 1, 1, 64, True), (3, 5, 2, 1, 128, True), (2, 7, 2, 2, 16, False),
+    (1, 1000, 2, 1, 128, True), (1, 513, 1, 1, 64, False),
 ])
 def test_prefill_f32_small(oracle, B, N, Hq, Hkv, d, causal):
     w = inputs.dense(B, N, Hq, Hkv, d, 2000 + N + d, torch.float32, causal=causal)
@@ -150,6 +155,43 @@ def test_prefill_f32_small(oracle, B, N, Hq, Hkv, d, causal):
     e = errors(f32(o), o_ref, f32(lse), lse_ref)
     assert_close(e, (B, N, Hq, Hkv, d, causal))
     assert e["max_o"] < 1e-4 and e["max_lse"] < 1e-4, e  # fp32 arithmetic throughout
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,d,causal", [
+    (1, 256, 1, 1, 64, False), (1, 1, 1, 1, 16, True), (2, 67, 4, 2, 128, True),
+    (1, 300, 2, 1, 96, False), (3, 130, 2, 2, 48, True), (1, 1100, 1, 1, 80, True),
+])
+def test_prefill_f32_both_tile_heights(oracle, B, N, Hq, Hkv, d, causal):
+    """16-row and 4-row CTAs (through the test hook) each match the oracle, and
+    attn_fwd_f32 returns, bit for bit, the result of the height its launch-size rule
+    picks: 4 rows when 16-row CTAs would fill at most half of the SMs."""
+    lib = A.load_library()
+    P = ctypes.c_void_p
+    fn = lib.attn_testing_fwd_f32_rows
+    fn.argtypes = [P, P, P, P, P] + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, P]
+    fn.restype = ctypes.c_int
+    w = inputs.dense(B, N, Hq, Hkv, d, 2100 + N + d, torch.float32, causal=causal)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    o_ref, lse_ref = oracle.attn_fwd(f32(w.q), f32(w.k), f32(w.v), causal, w.scale)
+    got = {}
+    for rows in (16, 4):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+        rc = fn(P(q.data_ptr()), P(k.data_ptr()), P(v.data_ptr()), P(o.data_ptr()),
+                P(lse.data_ptr()), B, Hq, Hkv, N, d, int(causal), w.scale, rows,
+                P(torch.cuda.current_stream().cuda_stream))
+        assert rc == 0, A.attn_status_string(rc)
+        torch.cuda.synchronize()
+        check_status()
+        e = errors(f32(o), o_ref, f32(lse), lse_ref)
+        assert_close(e, (rows, B, N, Hq, Hkv, d, causal))
+        assert e["max_o"] < 1e-4 and e["max_lse"] < 1e-4, (rows, e)
+        got[rows] = (o, lse)
+    o, lse = A.attn_fwd_f32(q, k, v, causal, w.scale)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pick = 4 if 2 * ((N + 15) // 16) * Hq * B <= sms else 16
+    assert torch.equal(o, got[pick][0]) and torch.equal(lse, got[pick][1]), pick
 
 
 # ---------------------------------------------------------------- varlen
