@@ -131,9 +131,12 @@ attn_status_t device_state(DeviceState **out) {
         if ((e = cudaFuncSetAttribute(prefill_simt_kernel,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)prefill_simt_smem_bytes(kSimtMaxD))) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(prefill_simt_rows4_kernel,
+            (e = cudaFuncSetAttribute(prefill_simt_rows_kernel<4>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)prefill_simt_rows4_smem_bytes(kSimtMaxD))) != cudaSuccess)
+                                      (int)prefill_simt_rows_smem_bytes(4, kSimtMaxD))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(prefill_simt_rows_kernel<2>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)prefill_simt_rows_smem_bytes(2, kSimtMaxD))) != cudaSuccess)
             return cuda_fail(e);
         if ((e = prefill_attrs<128>()) != cudaSuccess || (e = prefill_attrs<64>()) != cudaSuccess)
             return cuda_fail(e);
@@ -395,11 +398,11 @@ attn_status_t attn_fwd_chunked_paged(const void *q, const void *k_cache, const v
 
 namespace {
 
-// fp32 prefill with `rows` query rows per CTA: 16 (prefill_simt_kernel) or 4
-// (prefill_simt_rows4_kernel); 0 lets the launch size decide: 4-row CTAs when the
-// 16-row grid would fill at most half of the SMs (each SM then gets one or two
-// 4-row CTAs instead of leaving most SMs idle), 16-row CTAs otherwise (each K/V
-// tile loaded into shared memory then serves 16 rows).
+// fp32 prefill with `rows` query rows per CTA: 16 (prefill_simt_kernel), 4 or 2
+// (prefill_simt_rows_kernel<4>, <2>); 0 lets the launch size decide.  With C CTAs of
+// 16 rows: 2-row CTAs when 8 C <= #SM (one per SM at most), 4-row CTAs when
+// 2 C <= #SM (one or two per SM), else 16-row CTAs (each K/V tile loaded into shared
+// memory then serves 16 rows).  Smaller tiles put a short launch on more SMs.
 attn_status_t fwd_f32_impl(const float *q, const float *k, const float *v, float *o, float *lse,
                            int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                            int rows, attn_stream_t stream) {
@@ -407,7 +410,7 @@ attn_status_t fwd_f32_impl(const float *q, const float *k, const float *v, float
     if (B <= 0 || N <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
-    if (rows != 0 && rows != kSimtBM && rows != kSimt4BM) return ATTN_ERR_INVALID_ARG;
+    if (rows != 0 && rows != kSimtBM && rows != 4 && rows != 2) return ATTN_ERR_INVALID_ARG;
     if (d > kSimtMaxD || d % 16 != 0) return ATTN_ERR_UNSUPPORTED;
     if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
     DeviceState *st = nullptr;
@@ -429,12 +432,15 @@ attn_status_t fwd_f32_impl(const float *q, const float *k, const float *v, float
     p.scale_log2 = scale * kLog2e;
     if (rows == 0) {
         const long long ctas16 = (long long)((N + kSimtBM - 1) / kSimtBM) * Hq * B;
-        rows = 2 * ctas16 <= st->sms ? kSimt4BM : kSimtBM;
+        rows = 8 * ctas16 <= st->sms ? 2 : 2 * ctas16 <= st->sms ? 4 : kSimtBM;
     }
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    if (rows == kSimt4BM) {
-        dim3 grid((N + kSimt4BM - 1) / kSimt4BM, Hq, B);
-        prefill_simt_rows4_kernel<<<grid, kSimtThreads, prefill_simt_rows4_smem_bytes(d), cs>>>(p);
+    if (rows == 2) {
+        dim3 grid((N + 1) / 2, Hq, B);
+        prefill_simt_rows_kernel<2><<<grid, kSimtThreads, prefill_simt_rows_smem_bytes(2, d), cs>>>(p);
+    } else if (rows == 4) {
+        dim3 grid((N + 3) / 4, Hq, B);
+        prefill_simt_rows_kernel<4><<<grid, kSimtThreads, prefill_simt_rows_smem_bytes(4, d), cs>>>(p);
     } else {
         dim3 grid((N + kSimtBM - 1) / kSimtBM, Hq, B);
         prefill_simt_kernel<<<grid, kSimtThreads, prefill_simt_smem_bytes(d), cs>>>(p);
@@ -454,7 +460,7 @@ attn_status_t attn_testing_fwd_f32_rows(const float *q, const float *k, const fl
                                         float *lse, int B, int Hq, int Hkv, int N, int d,
                                         int causal, float scale, int rows,
                                         attn_stream_t stream) {
-    if (rows != kSimtBM && rows != kSimt4BM) return ATTN_ERR_INVALID_ARG;
+    if (rows != kSimtBM && rows != 4 && rows != 2) return ATTN_ERR_INVALID_ARG;
     return fwd_f32_impl(q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, rows, stream);
 }
 

@@ -16,9 +16,9 @@
 // - prefill_simt_kernel: 16 rows per CTA, 16 threads per row.  Each K/V tile
 //   loaded into shared memory serves 16 rows: the choice when the launch has
 //   enough CTAs to fill the GPU.
-// - prefill_simt_rows4_kernel: 4 rows per CTA, 64 threads per row, for launches
-//   that would leave most SMs idle with 16-row tiles (N = 256 on one head is 16
-//   such CTAs, or 64 of 4 rows).
+// - prefill_simt_rows_kernel<4> and <2>: 4 or 2 rows per CTA, 64 or 128 threads
+//   per row, for launches that would leave most SMs idle with 16-row tiles (N = 256
+//   on one head is 16 such CTAs, 64 of 4 rows or 128 of 2 rows).
 #pragma once
 
 #include "ptx.cuh"
@@ -28,11 +28,8 @@ namespace attn07 {
 constexpr int kSimtBM = 16;   // query rows per CTA (prefill_simt_kernel)
 constexpr int kSimtBN = 64;   // keys per tile
 constexpr int kSimtTPR = 16;  // threads per query row (prefill_simt_kernel)
-constexpr int kSimt4BM = 4;   // query rows per CTA (prefill_simt_rows4_kernel)
-constexpr int kSimt4TPR = 64; // threads per query row (prefill_simt_rows4_kernel)
 constexpr int kSimtThreads = kSimtBM * kSimtTPR;
 constexpr int kSimtMaxD = 128;
-static_assert(kSimt4BM * kSimt4TPR == kSimtThreads, "both thread maps use 256 threads");
 
 struct SimtParams {
     const float *q;
@@ -231,25 +228,34 @@ inline size_t prefill_simt_smem_bytes(int d) {
     return sizeof(float) * ((size_t)(kSimtBM + 2 * kSimtBN) * (d + 4) + kSimtBM * (kSimtBN + 4));
 }
 
-// 4 rows per CTA, 256 threads, 64 per query row (two warps).  Thread (row r, lane c
-// of its row):
-// - scores: key c of each 64-key tile, one dot product over d with the row's Q (a
-//   warp-wide broadcast) and key row c (32 rows per warp, conflict-free with the
-//   padded row length);
-// - output: columns c and c + 64 of its row (those below d), so that a warp's value
-//   loads are 32 consecutive words of one value row.
-// The row maximum and sum are warp shuffles, then one exchange between the row's two
+// ROWS = 4 or 2 rows per CTA, 256 threads, TPR = 64 or 128 per query row (two or
+// four warps).  Thread (row r, lane c of its row):
+// - scores: one key of each 64-key tile per S = TPR / 64 threads.  Each of a key's
+//   threads takes every S-th float4 of the dot product over d (the row's Q a
+//   warp-wide broadcast, the key rows conflict-free with the padded row length),
+//   and a shuffle adds the S partial sums.
+// - output: with 64 threads per row, columns c and c + 64 (those below d) over all
+//   keys of the tile; with 128, column c over all keys when d > 64, else column
+//   c % 64 over one half of the tile's keys (the halves added once at the end).
+//   A warp's value loads are 32 consecutive words of one value row.
+// The row maximum and sum are warp shuffles, then one exchange between the row's
 // warps through shared memory.  (One CTA per SM: the registers hold a K/V tile's
 // share and its slots' offsets.)
+template <int ROWS>
 __global__ void __launch_bounds__(kSimtThreads, 1)
-prefill_simt_rows4_kernel(const SimtParams p) {
+prefill_simt_rows_kernel(const SimtParams p) {
+    constexpr int TPR = kSimtThreads / ROWS;  // threads per query row
+    constexpr int S = TPR / kSimtBN;          // threads per key in the scores
+    constexpr int NW = TPR / 32;              // warps per row
+    static_assert(S == 1 || S == 2, "64 or 128 threads per row");
     extern __shared__ __align__(16) float smem_f[];
     const int dp = p.d + 4;  // padded row length (floats)
-    float *Qs = smem_f;                          // [4][dp]
-    float *Ks = Qs + kSimt4BM * dp;              // [64][dp]
+    float *Qs = smem_f;                          // [ROWS][dp]
+    float *Ks = Qs + ROWS * dp;                  // [64][dp]
     float *Vs = Ks + kSimtBN * dp;               // [64][dp]
-    float *Ps = Vs + kSimtBN * dp;               // [4][64]
-    float *red = Ps + kSimt4BM * kSimtBN;        // [2][4][2]: row maxima, row sums per warp
+    float *Ps = Vs + kSimtBN * dp;               // [ROWS][64]
+    float *red = Ps + ROWS * kSimtBN;            // [2][ROWS][NW]: row maxima, row sums per warp
+    float *half_o = red + 2 * ROWS * NW;         // [ROWS][64]: the second key half's output
 
     const int tile = blockIdx.x;
     const int h = blockIdx.y;
@@ -264,19 +270,30 @@ prefill_simt_rows4_kernel(const SimtParams p) {
         start = seq * p.N;
         len = p.N;
     }
-    const int row0 = tile * kSimt4BM;
+    const int row0 = tile * ROWS;
     if (row0 >= len) return;
 
     const int tid = threadIdx.x;
-    const int r = tid / kSimt4TPR;   // query row in tile
-    const int c = tid % kSimt4TPR;   // lane within the row: key c, output columns c, c + 64
-    const int half = c >> 5;         // the row's warp
+    const int r = tid / TPR;         // query row in tile
+    const int c = tid % TPR;         // lane within the row
+    const int wr = c >> 5;           // the row's warp
     const int lane = tid & 31;
+    // key of the scores and part of its dot product: with two parts, lanes l and l + 16
+    // of a warp share a key, so that each 8-lane phase of a 16-byte shared-memory load
+    // reads 8 different key rows (no bank conflict)
+    const int kc = S == 1 ? c : (c >> 5) * 16 + (lane & 15);
+    const int kp = S == 1 ? 0 : lane >> 4;
     const int d = p.d;
     const int nvec = d >> 2;         // float4 per row
+    // output: column col over keys [jlo_o, jlo_o + jn_o) of each tile (second column
+    // col + 64 with 64 threads per row)
+    const bool split_keys = S == 2 && d <= 64;
+    const int col = split_keys ? (c & 63) : c;
+    const int jlo_o = split_keys ? 32 * (c >> 6) : 0;
+    const int jn_o = split_keys ? 32 : kSimtBN;
 
     // Q tile, pre-scaled by scale*log2(e) so scores come out in log2 units.
-    for (int idx = tid; idx < kSimt4BM * nvec; idx += kSimtThreads) {
+    for (int idx = tid; idx < ROWS * nvec; idx += kSimtThreads) {
         const int rr = idx / nvec, cv = idx % nvec;
         float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row0 + rr < len) {
@@ -289,11 +306,11 @@ prefill_simt_rows4_kernel(const SimtParams p) {
     }
 
     float m = -INFINITY, l = 0.f;
-    float acc0 = 0.f, acc1 = 0.f;  // output columns c and c + 64
+    float acc0 = 0.f, acc1 = 0.f;  // output columns col and col + 64
 
     const int qi = row0 + r;  // this thread's query position
     int kv_end = len;
-    if (p.causal) kv_end = min(len, row0 + kSimt4BM);
+    if (p.causal) kv_end = min(len, row0 + ROWS);
 
     // the K and V tiles pass through registers: each thread's share of the next tile
     // is loaded from device memory while the current one is computed on (rows past
@@ -320,10 +337,11 @@ prefill_simt_rows4_kernel(const SimtParams p) {
         const int64_t base = ((int64_t)(start + t0) * p.Hkv + g) * d;
 #pragma unroll
         for (int i = 0; i < kMaxVec; ++i) {
-            pk[i] = pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (vrow[i] < lim) {
                 pk[i] = *reinterpret_cast<const float4 *>(p.k + base + goff[i]);
                 pv[i] = *reinterpret_cast<const float4 *>(p.v + base + goff[i]);
+            } else {
+                pk[i] = pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
     };
@@ -340,12 +358,13 @@ prefill_simt_rows4_kernel(const SimtParams p) {
         __syncthreads();
         if (kv0 + kSimtBN < kv_end) fetch(kv0 + kSimtBN);
 
-        // score of key c: four partial sums over d (one per float4 component)
+        // score of key kc: four partial sums (one per float4 component) over this
+        // thread's float4 groups, then the key's S parts added
         const float *qr = Qs + r * dp;
-        const float *kr = Ks + c * dp;
+        const float *kr = Ks + kc * dp;
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
-        for (int cc = 0; cc < d; cc += 4) {
+        for (int cc = 4 * kp; cc < d; cc += 4 * S) {
             const float4 qa = *reinterpret_cast<const float4 *>(qr + cc);
             const float4 ka = *reinterpret_cast<const float4 *>(kr + cc);
             a0 = fmaf(qa.x, ka.x, a0);
@@ -353,42 +372,52 @@ prefill_simt_rows4_kernel(const SimtParams p) {
             a2 = fmaf(qa.z, ka.z, a2);
             a3 = fmaf(qa.w, ka.w, a3);
         }
-        const int kj = kv0 + c;
+        float sc = (a0 + a1) + (a2 + a3);
+        if constexpr (S == 2) sc += __shfl_xor_sync(0xffffffffu, sc, 16);
+        const int kj = kv0 + kc;
         const bool ok = kj < len && (!p.causal || kj <= qi);
-        const float s = ok ? (a0 + a1) + (a2 + a3) : -INFINITY;
+        const float s = ok ? sc : -INFINITY;
 
-        // row maximum: the warp's, then the row's two warps' through shared memory
+        // row maximum: the warp's, then the row's warps' through shared memory
         float tmax = s;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-        if (lane == 0) red[r * 2 + half] = tmax;
+        if (lane == 0) red[r * NW + wr] = tmax;
         __syncthreads();
-        tmax = fmaxf(red[r * 2], red[r * 2 + 1]);
+        tmax = red[r * NW];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) tmax = fmaxf(tmax, red[r * NW + w]);
         const float m_new = fmaxf(m, tmax);
         // a row with no allowed key yet keeps m = -inf; shift by 0 then
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = ex2(m - m_use);
         const float pj = ex2(s - m_use);  // 0 for a masked key
-        Ps[r * kSimtBN + c] = pj;
-        float tsum = pj;
+        if (kp == 0) Ps[r * kSimtBN + kc] = pj;
+        // (each key counted once: by the first of its S threads)
+        float tsum = kp == 0 ? pj : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
-        if (lane == 0) red[8 + r * 2 + half] = tsum;
+        if (lane == 0) red[ROWS * NW + r * NW + wr] = tsum;
         __syncthreads();
-        l = l * alpha + (red[8 + r * 2] + red[8 + r * 2 + 1]);
+        float rsum = red[ROWS * NW + r * NW];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) rsum += red[ROWS * NW + r * NW + w];
+        l = l * alpha + rsum;
         m = m_new;
 
-        // O = O * alpha + P V over this thread's columns.  Keys from the tile's end up
-        // to the next multiple of 4 have P = 0 and finite (or zero-filled) values.
+        // O = O * alpha + P V over this thread's columns and keys.  Keys from the
+        // tile's end up to the next multiple of 4 have P = 0 and finite (or
+        // zero-filled) values.
         acc0 *= alpha;
         acc1 *= alpha;
         const int jmax = (min(kSimtBN, kv_end - kv0) + 3) & ~3;
+        const int j1 = min(jlo_o + jn_o, jmax);
         const float *pr = Ps + r * kSimtBN;
-        if (c + 64 < d) {
+        if (S == 1 && col + 64 < d) {
 #pragma unroll 2
-            for (int j = 0; j < jmax; j += 4) {
+            for (int j = jlo_o; j < j1; j += 4) {
                 const float4 p4 = *reinterpret_cast<const float4 *>(pr + j);
-                const float *vr = Vs + j * dp + c;
+                const float *vr = Vs + j * dp + col;
                 acc0 = fmaf(p4.x, vr[0], acc0);
                 acc1 = fmaf(p4.x, vr[64], acc1);
                 acc0 = fmaf(p4.y, vr[dp], acc0);
@@ -398,24 +427,37 @@ prefill_simt_rows4_kernel(const SimtParams p) {
                 acc0 = fmaf(p4.w, vr[3 * dp], acc0);
                 acc1 = fmaf(p4.w, vr[3 * dp + 64], acc1);
             }
-        } else if (c < d) {
+        } else if (col < d) {
+            // (two chains, even and odd keys)
 #pragma unroll 2
-            for (int j = 0; j < jmax; j += 4) {
+            for (int j = jlo_o; j < j1; j += 4) {
                 const float4 p4 = *reinterpret_cast<const float4 *>(pr + j);
-                const float *vr = Vs + j * dp + c;
+                const float *vr = Vs + j * dp + col;
                 acc0 = fmaf(p4.x, vr[0], acc0);
-                acc0 = fmaf(p4.y, vr[dp], acc0);
+                acc1 = fmaf(p4.y, vr[dp], acc1);
                 acc0 = fmaf(p4.z, vr[2 * dp], acc0);
-                acc0 = fmaf(p4.w, vr[3 * dp], acc0);
+                acc1 = fmaf(p4.w, vr[3 * dp], acc1);
             }
         }
     }
 
-    if (qi < len) {
+    // one column's partial outputs added: the even and odd key chains, and (keys split
+    // between two threads) the second half's through shared memory
+    float out0 = acc0, out1 = acc1;
+    if (!(S == 1 && col + 64 < d)) {
+        out0 = acc0 + acc1;
+        out1 = 0.f;
+    }
+    if (split_keys) {
+        if (jlo_o != 0 && col < d) half_o[r * kSimtBN + col] = out0;
+        __syncthreads();
+        if (jlo_o == 0 && col < d) out0 += half_o[r * kSimtBN + col];
+    }
+    if (qi < len && jlo_o == 0) {
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
         float *orow = p.o + ((int64_t)(start + qi) * p.Hq + h) * d;
-        if (c < d) orow[c] = acc0 * inv;
-        if (c + 64 < d) orow[c + 64] = acc1 * inv;
+        if (col < d) orow[col] = out0 * inv;
+        if (S == 1 && col + 64 < d) orow[col + 64] = out1 * inv;
         if (p.lse && c == 0) {
             const float lse = (l > 0.f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
             int64_t idx;
@@ -426,9 +468,10 @@ prefill_simt_rows4_kernel(const SimtParams p) {
     }
 }
 
-inline size_t prefill_simt_rows4_smem_bytes(int d) {
-    return sizeof(float) *
-           ((size_t)(kSimt4BM + 2 * kSimtBN) * (d + 4) + kSimt4BM * kSimtBN + 16);
+inline size_t prefill_simt_rows_smem_bytes(int rows, int d) {
+    const int nw = kSimtThreads / rows / 32;
+    return sizeof(float) * ((size_t)(rows + 2 * kSimtBN) * (d + 4) + 2 * (size_t)rows * kSimtBN +
+                            2 * (size_t)rows * nw);
 }
 
 }  // namespace attn07

@@ -165,7 +165,8 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "prefill_tc_kernel": ("prefill_tc.cuh", "ptx.cuh"),
     "prefill_simt_kernel": ("prefill_simt.cuh", "ptx.cuh"),
-    "prefill_simt_rows4_kernel": ("prefill_simt.cuh", "ptx.cuh"),
+    "prefill_simt_rows_kernel<4>": ("prefill_simt.cuh", "ptx.cuh"),
+    "prefill_simt_rows_kernel<2>": ("prefill_simt.cuh", "ptx.cuh"),
     "decode_split_kernel": ("decode.cuh", "ptx.cuh"),
     "decode_split_kernel<true>": ("decode.cuh", "ptx.cuh"),
 }
@@ -407,12 +408,16 @@ class Leg:
 
 
 def simt_kernel(q_shape, dev) -> str:
-    """The fp32 kernel attn_fwd_f32 launches for q of shape [B, N, Hq, d]: 4-row CTAs
-    when 16-row CTAs would fill at most half of the SMs, else 16-row CTAs."""
+    """The fp32 kernel attn_fwd_f32 launches for q of shape [B, N, Hq, d]: with C CTAs of
+    16 rows, 2-row CTAs when 8 C <= #SM, 4-row CTAs when 2 C <= #SM, else 16-row CTAs."""
     B, N, Hq, _ = q_shape
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    return ("prefill_simt_rows4_kernel" if 2 * ((N + 15) // 16) * Hq * B <= sms
-            else "prefill_simt_kernel")
+    ctas16 = ((N + 15) // 16) * Hq * B
+    if 8 * ctas16 <= sms:
+        return "prefill_simt_rows_kernel<2>"
+    if 2 * ctas16 <= sms:
+        return "prefill_simt_rows_kernel<4>"
+    return "prefill_simt_kernel"
 
 
 def launches_per_call(leg) -> int:

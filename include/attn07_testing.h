@@ -33,8 +33,8 @@ attn_status_t attn_testing_decode_paged_ctas(const void *q, const void *k_cache,
 
 /*
  * attn_fwd_f32 with a fixed tile height: `rows` = 16 (16 query rows per CTA,
- * 16 threads per row) or 4 (4 rows per CTA, 64 threads per row) instead of the
- * library's choice by launch size.  Both compute the same attention formula
+ * 16 threads per row), 4 (4 rows per CTA, 64 threads per row) or 2 (2 rows per
+ * CTA, 128 threads per row) instead of the library's choice by launch size.  Both compute the same attention formula
  * (the fatihsoysal.com page, section "Transformer Mimarisi ve Self-Attention
  * Mekanizması") with the online softmax of section "Online Softmax Prensibi",
  * in fp32; their results differ only by the order of fp32 additions.

@@ -117,14 +117,14 @@ def test_f32_head_dim_rule(lib):
 
 
 def test_f32_rows_hook_takes_the_two_tile_heights(lib):
-    """attn_testing_fwd_f32_rows runs 16-row or 4-row CTAs; any other height is refused
+    """attn_testing_fwd_f32_rows runs 16-, 4- or 2-row CTAs; any other height is refused
     before anything is launched, and the shared argument rules still apply."""
     P = ctypes.c_void_p
     p = P(1 << 20)
     fn = lib.attn_testing_fwd_f32_rows
     fn.argtypes = [P, P, P, P, P] + [ctypes.c_int] * 6 + [ctypes.c_float, ctypes.c_int, P]
     fn.restype = ctypes.c_int
-    for rows in (0, 1, 8, 32, -4):
+    for rows in (0, 1, 3, 8, 32, -4):
         assert fn(p, p, p, p, None, 1, 1, 1, 8, 64, 1, 0.1, rows, None) == A.ATTN_ERR_INVALID_ARG
     assert fn(None, p, p, p, None, 1, 1, 1, 8, 64, 1, 0.1, 4, None) == A.ATTN_ERR_INVALID_ARG
     assert fn(p, p, p, p, None, 1, 1, 1, 8, 24, 1, 0.1, 16, None) == A.ATTN_ERR_UNSUPPORTED

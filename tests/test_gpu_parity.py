@@ -162,9 +162,9 @@ def test_prefill_f32_small(oracle, B, N, Hq, Hkv, d, causal):
     (1, 300, 2, 1, 96, False), (3, 130, 2, 2, 48, True), (1, 1100, 1, 1, 80, True),
 ])
 def test_prefill_f32_both_tile_heights(oracle, B, N, Hq, Hkv, d, causal):
-    """16-row and 4-row CTAs (through the test hook) each match the oracle, and
+    """16-, 4- and 2-row CTAs (through the test hook) each match the oracle, and
     attn_fwd_f32 returns, bit for bit, the result of the height its launch-size rule
-    picks: 4 rows when 16-row CTAs would fill at most half of the SMs."""
+    picks: with C CTAs of 16 rows, 2 rows when 8 C <= #SM, 4 rows when 2 C <= #SM."""
     lib = A.load_library()
     P = ctypes.c_void_p
     fn = lib.attn_testing_fwd_f32_rows
@@ -174,7 +174,7 @@ def test_prefill_f32_both_tile_heights(oracle, B, N, Hq, Hkv, d, causal):
     q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
     o_ref, lse_ref = oracle.attn_fwd(f32(w.q), f32(w.k), f32(w.v), causal, w.scale)
     got = {}
-    for rows in (16, 4):
+    for rows in (16, 4, 2):
         o = torch.empty_like(q)
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
         rc = fn(P(q.data_ptr()), P(k.data_ptr()), P(v.data_ptr()), P(o.data_ptr()),
@@ -190,7 +190,8 @@ def test_prefill_f32_both_tile_heights(oracle, B, N, Hq, Hkv, d, causal):
     o, lse = A.attn_fwd_f32(q, k, v, causal, w.scale)
     torch.cuda.synchronize()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    pick = 4 if 2 * ((N + 15) // 16) * Hq * B <= sms else 16
+    ctas16 = ((N + 15) // 16) * Hq * B
+    pick = 2 if 8 * ctas16 <= sms else 4 if 2 * ctas16 <= sms else 16
     assert torch.equal(o, got[pick][0]) and torch.equal(lse, got[pick][1]), pick
 
 
