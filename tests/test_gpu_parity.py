@@ -161,7 +161,7 @@ def test_prefill_f32_small(oracle, B, N, Hq, Hkv, d, causal):
     (1, 256, 1, 1, 64, False), (1, 1, 1, 1, 16, True), (2, 67, 4, 2, 128, True),
     (1, 300, 2, 1, 96, False), (3, 130, 2, 2, 48, True), (1, 1100, 1, 1, 80, True),
 ])
-def test_prefill_f32_both_tile_heights(oracle, B, N, Hq, Hkv, d, causal):
+def test_prefill_f32_every_tile_height(oracle, B, N, Hq, Hkv, d, causal):
     """16-, 4- and 2-row CTAs (through the test hook) each match the oracle, and
     attn_fwd_f32 returns, bit for bit, the result of the height its launch-size rule
     picks: with C CTAs of 16 rows, 2 rows when 8 C <= #SM, 4 rows when 2 C <= #SM."""
