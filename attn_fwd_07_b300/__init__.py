@@ -20,6 +20,7 @@ __all__ = [
     "attn_fwd_two_pass",
     "attn_fwd_f32",
     "attn_fwd_varlen", "attn_decode_paged", "attn_decode_paged_window", "attn_decode_paged_fp8",
+    "attn_decode_paged_int8",
     "attn_decode_paged_noalloc", "attn_decode_workspace_size", "attn_status_string",
     "attn_get_device_status", "attn_version", "attn_last_cuda_error",
 ]
@@ -68,6 +69,8 @@ def load_library(path: str = LIB_PATH):
                                                I, I, F, P]
         lib.attn_decode_paged_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
                                               P, SZ, P]
+        lib.attn_decode_paged_int8.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
+                                               P, SZ, P]
         lib.attn_decode_paged_window.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F,
                                                  P, SZ, P]
         lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F,
@@ -83,6 +86,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_last_cuda_error.restype = ctypes.c_char_p
         for name in ("attn_fwd", "attn_fwd_f32", "attn_fwd_varlen", "attn_decode_paged",
                      "attn_fwd_window", "attn_decode_paged_window", "attn_decode_paged_fp8",
+                     "attn_decode_paged_int8",
                      "attn_fwd_chunked_paged", "attn_fwd_two_pass",
                      "attn_decode_paged_noalloc", "attn_get_device_status", "attn_fwd_host",
                      "attn_release_host_staging", "attn_selftest_wait_timeout"):
@@ -348,15 +352,11 @@ def attn_decode_paged(q, k_cache, v_cache, page_table, seq_lens, scale: float | 
     return o, lse
 
 
-def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
-                          scale: float | None = None, o=None, lse=None, workspace=None,
-                          want_lse: bool = True, stream=None):
-    """Decode against an FP8 E4M3 paged cache: k_cache/v_cache uint8 [P,page,Hkv,d] holding
-    E4M3 bytes, k_scale/v_scale float32 [Hkv] per-head scales.  q, page_table, seq_lens and
-    the results as attn_decode_paged."""
+def _decode_paged_bytes(entry, name, cache_dtype, q, k_cache, v_cache, k_scale, v_scale,
+                        page_table, seq_lens, scale, o, lse, workspace, want_lse, stream):
     _need(q, torch.bfloat16, "q")
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, torch.uint8, n)
+        _need(t, cache_dtype, n)
     for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
         _need(t, torch.float32, n)
     _need(page_table, torch.int32, "page_table")
@@ -373,12 +373,34 @@ def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq
     need = attn_decode_workspace_size(B, Hq, d, maxp, ps)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    rc = load_library().attn_decode_paged_fp8(
+    rc = entry(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
         _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq, Hkv, d, ps, P, maxp, float(scale),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(rc, "attn_decode_paged_fp8")
+    _check(rc, name)
     return o, lse
+
+
+def attn_decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                          scale: float | None = None, o=None, lse=None, workspace=None,
+                          want_lse: bool = True, stream=None):
+    """Decode against an FP8 E4M3 paged cache: k_cache/v_cache uint8 [P,page,Hkv,d] holding
+    E4M3 bytes, k_scale/v_scale float32 [Hkv] per-head scales.  q, page_table, seq_lens and
+    the results as attn_decode_paged."""
+    return _decode_paged_bytes(load_library().attn_decode_paged_fp8, "attn_decode_paged_fp8",
+                               torch.uint8, q, k_cache, v_cache, k_scale, v_scale, page_table,
+                               seq_lens, scale, o, lse, workspace, want_lse, stream)
+
+
+def attn_decode_paged_int8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                           scale: float | None = None, o=None, lse=None, workspace=None,
+                           want_lse: bool = True, stream=None):
+    """Decode against an INT8 paged cache: k_cache/v_cache int8 [P,page,Hkv,d],
+    k_scale/v_scale float32 [Hkv] per-head scales (element c of head g stands for
+    scale[g] * int8).  q, page_table, seq_lens and the results as attn_decode_paged."""
+    return _decode_paged_bytes(load_library().attn_decode_paged_int8, "attn_decode_paged_int8",
+                               torch.int8, q, k_cache, v_cache, k_scale, v_scale, page_table,
+                               seq_lens, scale, o, lse, workspace, want_lse, stream)
 
 
 def attn_decode_paged_window(q, k_cache, v_cache, page_table, seq_lens, window: int,

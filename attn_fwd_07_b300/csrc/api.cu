@@ -140,11 +140,13 @@ attn_status_t device_state(DeviceState **out) {
             return cuda_fail(e);
         if ((e = prefill_attrs<128>()) != cudaSuccess || (e = prefill_attrs<64>()) != cudaSuccess)
             return cuda_fail(e);
-        if ((e = cudaFuncSetAttribute(decode_split_kernel<true>,
+        if ((e = cudaFuncSetAttribute(decode_split_kernel<kCacheFp8>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      227 * 1024)) != cudaSuccess)
-            return cuda_fail(e);
-        if ((e = cudaFuncSetAttribute(decode_split_kernel<false>,
+                                      227 * 1024)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(decode_split_kernel<kCacheInt8>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      227 * 1024)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(decode_split_kernel<kCacheBf16>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       227 * 1024)) != cudaSuccess)
             return cuda_fail(e);
@@ -480,19 +482,20 @@ size_t attn_decode_workspace_size(int B, int Hq, int d, int max_pages_per_seq, i
 namespace {
 
 // The paged decode behind attn_decode_paged (window = -1), attn_decode_paged_window
-// (the query sees the last window + 1 tokens) and attn_decode_paged_fp8 (k_scale,
-// v_scale non-null: the cache holds FP8 E4M3 bytes).
+// (the query sees the last window + 1 tokens), attn_decode_paged_fp8 and
+// attn_decode_paged_int8 (cache = kCacheFp8 / kCacheInt8: the cache holds one byte per
+// element, k_scale and v_scale its per-head scales).
 attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *v_cache,
-                                const float *k_scale, const float *v_scale,
+                                const float *k_scale, const float *v_scale, int cache,
                                 const int32_t *page_table, const int32_t *seq_lens, void *o,
                                 float *lse, int B, int Hq, int Hkv, int d, int page_size,
                                 int num_pages, int max_pages_per_seq, int window, float scale,
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream,
                                 int ctas = 0) {
-    const bool fp8 = k_scale != nullptr;
+    const bool byte = cache != kCacheBf16;
     if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !o || !workspace)
         return ATTN_ERR_INVALID_ARG;
-    if (fp8 && !v_scale) return ATTN_ERR_INVALID_ARG;
+    if (byte && (!k_scale || !v_scale)) return ATTN_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0 ||
         num_pages <= 0 || max_pages_per_seq <= 0)
         return ATTN_ERR_INVALID_ARG;
@@ -502,30 +505,30 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
         return ATTN_ERR_INVALID_ARG;
     if (page_size != kDecPage || (d != 64 && d != 128) || Hkv > kDecMaxHkv || Hq / Hkv > 8)
         return ATTN_ERR_UNSUPPORTED;
-    if (fp8 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (byte && d != 128) return ATTN_ERR_UNSUPPORTED;
     DeviceState *st = nullptr;
     attn_status_t s = device_state(&st);
     if (s != ATTN_OK) return s;
     const size_t need = attn_decode_workspace_size(B, Hq, d, max_pages_per_seq, page_size);
     if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
-    const size_t stage = dec_stage_bytes(Hkv, d, fp8);
-    // FP8 pages are half the bytes and twice the conversion work per byte: two CTAs per
-    // SM (sixteen consumer warps) with half the ring each hide more of the consumers'
-    // latency; the bf16 kernel keeps one CTA per SM and the deeper ring
-    const int ctas_per_sm = fp8 ? 2 : 1;
-    int stages = (int)(((fp8 ? 108 : 220) * 1024 - 2048) / stage);
+    const size_t stage = dec_stage_bytes(Hkv, d, byte);
+    // one-byte pages are half the bytes and twice the conversion work per byte: two
+    // CTAs per SM (sixteen consumer warps) with half the ring each hide more of the
+    // consumers' latency; the bf16 kernel keeps one CTA per SM and the deeper ring
+    const int ctas_per_sm = byte ? 2 : 1;
+    int stages = (int)(((byte ? 108 : 220) * 1024 - 2048) / stage);
     if (stages > kDecMaxStages) stages = kDecMaxStages;
     if (stages < 2) return ATTN_ERR_UNSUPPORTED;
     // cache as a 4-D tensor: (dim, token-in-page, head, page) so that one box
     // lands in shared memory as [head][token][128-byte row]: 64 bf16 dims per box,
-    // or all 128 E4M3 dims
-    const cuuint64_t esz = fp8 ? 1 : 2;
+    // or all 128 one-byte dims
+    const cuuint64_t esz = byte ? 1 : 2;
     const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)page_size, (cuuint64_t)Hkv,
                                 (cuuint64_t)num_pages};
     const cuuint64_t strides[3] = {(cuuint64_t)Hkv * d * esz, (cuuint64_t)d * esz,
                                    (cuuint64_t)page_size * Hkv * d * esz};
-    const cuuint32_t box[4] = {fp8 ? 128u : 64u, (cuuint32_t)page_size, (cuuint32_t)Hkv, 1};
-    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+    const cuuint32_t box[4] = {byte ? 128u : 64u, (cuuint32_t)page_size, (cuuint32_t)Hkv, 1};
+    const CUtensorMapDataType dt = byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap mk, mv;
     if ((s = make_map(&mk, k_cache, 4, dims, strides, box, dt)) != ATTN_OK) return s;
@@ -557,11 +560,13 @@ attn_status_t decode_paged_impl(const void *q, const void *k_cache, const void *
     // the workspace has a slot per CTA for up to kDecMaxCtasPerSm CTAs per SM
     if (ctas < 0 || ctas > kDecMaxCtasPerSm * st->sms) return ATTN_ERR_UNSUPPORTED;
     const int G = ctas > 0 ? ctas : st->sms * ctas_per_sm;
-    const size_t smem = dec_smem_bytes(Hkv, d, stages, fp8);
-    if (fp8)
-        decode_split_kernel<true><<<G, 32 * Hkv, smem, cs>>>(p, mk, mv);
+    const size_t smem = dec_smem_bytes(Hkv, d, stages, byte);
+    if (cache == kCacheFp8)
+        decode_split_kernel<kCacheFp8><<<G, 32 * Hkv, smem, cs>>>(p, mk, mv);
+    else if (cache == kCacheInt8)
+        decode_split_kernel<kCacheInt8><<<G, 32 * Hkv, smem, cs>>>(p, mk, mv);
     else
-        decode_split_kernel<false><<<G, 32 * Hkv, smem, cs>>>(p, mk, mv);
+        decode_split_kernel<kCacheBf16><<<G, 32 * Hkv, smem, cs>>>(p, mk, mv);
     if ((s = launch_status()) != ATTN_OK) return s;
     // the merge as a programmatic dependent of the split kernel: it is scheduled while
     // the split kernel's last CTAs run and waits on the device for their results, which
@@ -590,7 +595,8 @@ attn_status_t attn_decode_paged(const void *q, const void *k_cache, const void *
                                 float *lse, int B, int Hq, int Hkv, int d, int page_size,
                                 int num_pages, int max_pages_per_seq, float scale,
                                 void *workspace, size_t workspace_bytes, attn_stream_t stream) {
-    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, page_table, seq_lens, o, lse,
+    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, kCacheBf16, page_table,
+                             seq_lens, o, lse,
                              B, Hq, Hkv, d,
                              page_size, num_pages, max_pages_per_seq, -1, scale, workspace,
                              workspace_bytes, stream);
@@ -604,9 +610,22 @@ attn_status_t attn_decode_paged_fp8(const void *q, const void *k_cache, const vo
                                     void *workspace, size_t workspace_bytes,
                                     attn_stream_t stream) {
     if (!k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
-    return decode_paged_impl(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, o, lse,
-                             B, Hq, Hkv, d, page_size, num_pages, max_pages_per_seq, -1, scale,
-                             workspace, workspace_bytes, stream);
+    return decode_paged_impl(q, k_cache, v_cache, k_scale, v_scale, kCacheFp8, page_table,
+                             seq_lens, o, lse, B, Hq, Hkv, d, page_size, num_pages,
+                             max_pages_per_seq, -1, scale, workspace, workspace_bytes, stream);
+}
+
+attn_status_t attn_decode_paged_int8(const void *q, const void *k_cache, const void *v_cache,
+                                     const float *k_scale, const float *v_scale,
+                                     const int32_t *page_table, const int32_t *seq_lens, void *o,
+                                     float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                                     int num_pages, int max_pages_per_seq, float scale,
+                                     void *workspace, size_t workspace_bytes,
+                                     attn_stream_t stream) {
+    if (!k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
+    return decode_paged_impl(q, k_cache, v_cache, k_scale, v_scale, kCacheInt8, page_table,
+                             seq_lens, o, lse, B, Hq, Hkv, d, page_size, num_pages,
+                             max_pages_per_seq, -1, scale, workspace, workspace_bytes, stream);
 }
 
 attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const void *v_cache,
@@ -616,7 +635,8 @@ attn_status_t attn_decode_paged_window(const void *q, const void *k_cache, const
                                        int window, float scale, void *workspace,
                                        size_t workspace_bytes, attn_stream_t stream) {
     if (window < -1) return ATTN_ERR_INVALID_ARG;
-    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, page_table, seq_lens, o, lse,
+    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, kCacheBf16, page_table,
+                             seq_lens, o, lse,
                              B, Hq, Hkv, d,
                              page_size, num_pages, max_pages_per_seq, window, scale, workspace,
                              workspace_bytes, stream);
@@ -635,7 +655,8 @@ attn_status_t attn_testing_decode_paged_ctas(const void *q, const void *k_cache,
                                              size_t workspace_bytes, int ctas,
                                              attn_stream_t stream) {
     if (ctas <= 0) return ATTN_ERR_INVALID_ARG;
-    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, page_table, seq_lens, o, lse,
+    return decode_paged_impl(q, k_cache, v_cache, nullptr, nullptr, kCacheBf16, page_table,
+                             seq_lens, o, lse,
                              B, Hq, Hkv, d, page_size, num_pages, max_pages_per_seq, -1, scale,
                              workspace, workspace_bytes, stream, ctas);
 }

@@ -31,12 +31,12 @@
 // ldmatrix.  There is no producer warp: every warp walks the CTA's page stream,
 // the ring is kept S pages ahead, and the warp that releases a page's stage last
 // refills it with the page S further on (its id read while the page was being
-// attended).  The CTA is one warp per key/value head, so two CTAs of the FP8
-// kernel fit an SM at 128 registers a thread.  Each warp computes
-// S = q K^T and O += P V for its Hq/Hkv query heads with mma.sync m16n8k16
-// (bf16 in, fp32 accumulate; the query heads fill the first rows of the
-// 16-row tile).  The decode is bound by device-memory bandwidth: the
-// contraction per byte is small, and the ring keeps enough bytes in flight.
+// attended).  The CTA is one warp per key/value head, so two CTAs of the
+// one-byte-cache (FP8 or INT8) kernels fit an SM at 128 registers a thread.
+// Each warp computes S = q K^T and O += P V for its Hq/Hkv query heads with
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate; the query heads fill the first
+// rows of the 16-row tile).  The decode is bound by device-memory bandwidth:
+// the contraction per byte is small, and the ring keeps enough bytes in flight.
 #pragma once
 
 #include "ptx.cuh"
@@ -46,7 +46,7 @@ namespace attn07 {
 constexpr int kDecPage = 16;          // tokens per page (the kernel is built for it)
 constexpr int kDecMaxStages = 8;
 constexpr int kDecMaxHkv = 8;
-constexpr int kDecMaxCtasPerSm = 2;    // the FP8 kernel runs two CTAs per SM
+constexpr int kDecMaxCtasPerSm = 2;    // the one-byte-cache kernels run two CTAs per SM
 
 struct DecodeParams {
     const __nv_bfloat16 *q;    // [B, Hq, d]
@@ -56,7 +56,7 @@ struct DecodeParams {
     float *part_lse;           // [B + G, Hq]
     __nv_bfloat16 *o;          // [B, Hq, d]
     float *lse;                // [B, Hq] or null
-    const float *k_scale;      // FP8 cache: [Hkv] per-head scales of K and V; else null
+    const float *k_scale;      // one-byte cache: [Hkv] per-head scales of K and V; else null
     const float *v_scale;
     unsigned *status;
     int B, Hq, Hkv, d, num_pages, maxp;
@@ -78,7 +78,7 @@ static_assert(sizeof(DecodeStageMeta) * kDecMaxStages <= 160, "stage metadata mu
 // Shared-memory layout (offsets from a 1024-byte-aligned base):
 //   stage s:  bf16 cache: K half 0 .. K half (d/64 - 1), V half 0 .. V half (d/64 - 1),
 //             each [Hkv][16][64] bf16 = Hkv * 2048 bytes;
-//             FP8 cache (d = 128): K, then V, each [Hkv][16][128] bytes = Hkv * 2048
+//             one-byte cache (d = 128): K, then V, each [Hkv][16][128] bytes = Hkv * 2048
 //   then full[kDecMaxStages], empty[kDecMaxStages] mbarriers, meta, release counts,
 //   scalars (1 KB).
 __host__ __device__ inline uint32_t dec_half_bytes(int Hkv) { return (uint32_t)Hkv * 16u * 128u; }
@@ -129,24 +129,53 @@ __host__ __device__ __forceinline__ bool dec_range_nonempty(long long c, long lo
     return (c + 1) * T / G > c * T / G;
 }
 
-// FP8: the cache holds E4M3 bytes.  Each consumer lane reads the bytes of its MMA
-// fragments straight from the stage (the contraction's k order and the output's
-// column order are permuted so that they are contiguous 16-byte chunks), widens
-// them to f16 (exact) and runs the products with f16 operands; per-head scales
-// multiply the scores and the output.
-template <bool FP8>
-__global__ void __launch_bounds__(32 * kDecMaxHkv, FP8 ? 2 : 1)
+// The cache's element format: bf16, or one byte with a per-head scale (FP8 E4M3 or
+// INT8, value = scale[head] * byte value).
+enum : int { kCacheBf16 = 0, kCacheFp8 = 1, kCacheInt8 = 2 };
+
+// Four signed bytes (INT8) -> their values as two f16 pairs (bytes 0, 1 and bytes
+// 2, 3), exactly.  An f16 whose high byte is 0x64 (biased exponent 25, i.e. 2^10)
+// has unit spacing on [1024, 2048): with the low byte u it is 1024 + u.  Flipping a
+// byte's sign bit gives u = v + 128 for the signed value v, so the f16 holding
+// 1024 + u, minus 1152 (0x6480), is v; every step is exact.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = x ^ 0x80808080u;
+    const uint32_t a = prmt(u, 0x64646464u, 0x4140u);  // bytes 0, 1 over 0x64
+    const uint32_t b = prmt(u, 0x64646464u, 0x4342u);  // bytes 2, 3 over 0x64
+    const uint32_t off = 0x64806480u;                  // 1152 in both halves
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(off));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(off));
+}
+
+// Four cache bytes -> their values (exactly, as f16) in two f16 pairs: bytes 0 and 1,
+// bytes 2 and 3.
+template <int CACHE>
+__device__ __forceinline__ void dec_byte4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    if constexpr (CACHE == kCacheFp8)
+        e4m3x4_to_f16x2x2(x, lo, hi);
+    else
+        s8x4_to_f16x2x2(x, lo, hi);
+}
+
+// One-byte cache (FP8 E4M3 or INT8 bytes).  Each consumer lane reads the bytes of
+// its MMA fragments straight from the stage (the contraction's k order and the
+// output's column order are permuted so that they are contiguous 16-byte chunks),
+// widens them to f16 (exact for both formats) and runs the products with f16
+// operands; per-head scales multiply the scores and the output.
+template <int CACHE>
+__global__ void __launch_bounds__(32 * kDecMaxHkv, CACHE != kCacheBf16 ? 2 : 1)
 decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
+    constexpr bool BYTE = CACHE != kCacheBf16;  // a one-byte cache
     extern __shared__ uint8_t dec_smem_raw[];
     const uint32_t raw = smem_u32(dec_smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *base_ptr = dec_smem_raw + (base - raw);
 
     const int S = p.stages;
-    const uint32_t stage_bytes = dec_stage_bytes(p.Hkv, p.d, FP8);
+    const uint32_t stage_bytes = dec_stage_bytes(p.Hkv, p.d, BYTE);
     const uint32_t half_bytes = dec_half_bytes(p.Hkv);
-    const int nhalf = FP8 ? 1 : p.d / 64;   // TMA boxes per tensor and page
+    const int nhalf = BYTE ? 1 : p.d / 64;  // TMA boxes per tensor and page
     const uint32_t ctrl = base + (uint32_t)S * stage_bytes;
     uint8_t *ctrl_ptr = base_ptr + (size_t)S * stage_bytes;
     // control block: full[8] @0, empty[8] @64, meta[8] @128, released[8] @288,
@@ -296,7 +325,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         const int nk = p.d / 16;               // k-steps of S = q K^T
         const int nd = p.d / 8;                // n-tiles of O
 
-        // A fragments of q (rows 0..7).  FP8 cache: the k-slots of each 16-dim step
+        // A fragments of q (rows 0..7).  One-byte cache: the k-slots of each 16-dim step
         // are permuted so that a lane's K bytes are contiguous -- in half hf, k-step
         // 4 hf + j takes dims 16 (2 quad + hf) + 4 j .. + 3 for this lane's slots
         // (2 quad, 2 quad + 1, 2 quad + 8, 2 quad + 9); q uses the same permutation.
@@ -305,9 +334,10 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
         // and 2i + 1, whose swizzles differ in the lowest bit) fall in distinct banks.
         uint32_t qa[8][2];
         float oacc[16][4];
-        // scores are q . k * scale (* the head's key scale for an FP8 cache), log2 units
-        const float sl2 = FP8 ? p.scale_log2 * p.k_scale[g] : p.scale_log2;
-        const float vsc = FP8 ? p.v_scale[g] : 1.f;
+        // scores are q . k * scale (* the head's key scale for a one-byte cache), log2
+        // units
+        const float sl2 = BYTE ? p.scale_log2 * p.k_scale[g] : p.scale_log2;
+        const float vsc = BYTE ? p.v_scale[g] : 1.f;
         float m_run = -INFINITY, l_run = 0.f, q_run = 0.f;
         int cur_b = 0;
 
@@ -329,7 +359,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 for (int ks = 0; ks < 8; ++ks) {
                     if (ks < nk && row_ok) {
                         const uint32_t *qr = reinterpret_cast<const uint32_t *>(qb + row * p.d);
-                        if constexpr (FP8) {
+                        if constexpr (BYTE) {
                             const int d0 = 32 * quad + 16 * (ks >> 2) + 4 * (ks & 3);
                             qa[ks][0] = bf16x2_to_f16x2(qr[d0 >> 1]);
                             qa[ks][1] = bf16x2_to_f16x2(qr[(d0 + 2) >> 1]);
@@ -354,7 +384,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
             if (mt.ntok > 0) {
                 // ---- S = q K^T over the 16 tokens (two n-tiles of 8 tokens)
                 float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                if constexpr (FP8) {
+                if constexpr (BYTE) {
                     // token 8 nt + row: one 16-byte chunk per half holds this lane's dims;
                     // odd k-steps accumulate apart (two shorter dependency chains)
                     float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -369,7 +399,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 uint32_t b0, b1;
-                                e4m3x4_to_f16x2x2(wj[j], b0, b1);
+                                dec_byte4_to_f16x2x2<CACHE>(wj[j], b0, b1);
                                 mma_f16_16816((j & 1) ? sodd[nt] : sacc[nt], qa[4 * hf + j][0], 0u,
                                               qa[4 * hf + j][1], 0u, b0, b1);
                             }
@@ -425,11 +455,11 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 float pr[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) pr[j] = ex2(sv[j] - m_use);
-                // P enters the PV product as bf16 (f16 for an FP8 cache); O is normalised
+                // P enters the PV product as bf16 (f16 for a one-byte cache); O is normalised
                 // by the sum of the same rounded values, the log-sum-exp by the exact sum
-                const uint32_t pa0 = FP8 ? pack_f16(pr[0], pr[1]) : pack_bf16(pr[0], pr[1]);
-                const uint32_t pa2 = FP8 ? pack_f16(pr[2], pr[3]) : pack_bf16(pr[2], pr[3]);
-                float pq = FP8 ? (f16lo(pa0) + f16hi(pa0)) + (f16lo(pa2) + f16hi(pa2))
+                const uint32_t pa0 = BYTE ? pack_f16(pr[0], pr[1]) : pack_bf16(pr[0], pr[1]);
+                const uint32_t pa2 = BYTE ? pack_f16(pr[2], pr[3]) : pack_bf16(pr[2], pr[3]);
+                float pq = BYTE ? (f16lo(pa0) + f16hi(pa0)) + (f16lo(pa2) + f16hi(pa2))
                                : (bf16lo(pa0) + bf16hi(pa0)) + (bf16lo(pa2) + bf16hi(pa2));
                 float ps = (pr[0] + pr[1]) + (pr[2] + pr[3]);
                 pq += __shfl_xor_sync(0xffffffffu, pq, 1);
@@ -440,7 +470,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 q_run = q_run * alpha + pq;   // sum of the rounded P -> normalises O
                 if (!any_need) {
                     // no row of the warp moved its reference: O stands
-                } else if constexpr (FP8) {
+                } else if constexpr (BYTE) {
                     // O^T tiles: columns are query heads 2 quad and 2 quad + 1, whose
                     // factors live in lanes 8 quad and 8 quad + 4
                     const float ae = __shfl_sync(0xffffffffu, alpha, 8 * quad);
@@ -460,7 +490,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                     }
                 }
                 // ---- O += P V
-                if constexpr (FP8) {
+                if constexpr (BYTE) {
                     // O^T += V^T P^T: M = 16 dims, N = 8 query heads, K = the 16 tokens.
                     // This lane's P fragments (tokens 2 quad, +1, +8, +9 of head `row`) are
                     // the B fragments as they stand.  M-tile mt's rows `row` and `row` + 8
@@ -480,10 +510,10 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                     for (int wi = 0; wi < 4; ++wi) {
                         // m-tile 2 wi: bytes 0 (row) and 1 (row + 8); m-tile 2 wi + 1: bytes 2, 3
                         uint32_t e0, e1, e2, e3, f0, f1, f2, f3;
-                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x5140u), e0, e1);
-                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x5140u), e2, e3);
-                        e4m3x4_to_f16x2x2(prmt(a4[wi], b4[wi], 0x7362u), f0, f1);
-                        e4m3x4_to_f16x2x2(prmt(c4[wi], d4[wi], 0x7362u), f2, f3);
+                        dec_byte4_to_f16x2x2<CACHE>(prmt(a4[wi], b4[wi], 0x5140u), e0, e1);
+                        dec_byte4_to_f16x2x2<CACHE>(prmt(c4[wi], d4[wi], 0x5140u), e2, e3);
+                        dec_byte4_to_f16x2x2<CACHE>(prmt(a4[wi], b4[wi], 0x7362u), f0, f1);
+                        dec_byte4_to_f16x2x2<CACHE>(prmt(c4[wi], d4[wi], 0x7362u), f2, f3);
                         mma_f16_16816(oacc[2 * wi], e0, e1, e2, e3, pa0, pa2);
                         mma_f16_16816(oacc[2 * wi + 1], f0, f1, f2, f3, pa0, pa2);
                     }
@@ -522,7 +552,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
             if (mt.last) {
                 // ---- partial result of this segment -> workspace slot b + cta
                 const long long slot = (long long)cur_b + blockIdx.x;
-                if constexpr (FP8) {
+                if constexpr (BYTE) {
                     // O^T: this lane holds heads 2 quad (c0, c2) and 2 quad + 1 (c1, c3)
                     // at dims 16 row + 2 mt, + 1
                     const float qe = __shfl_sync(0xffffffffu, q_run, 8 * quad);
@@ -543,7 +573,7 @@ decode_split_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm
                 }
                 if (row_ok) {
                     const int h = g * Gq + row;
-                    if constexpr (!FP8) {
+                    if constexpr (!BYTE) {
                         const float inv = (q_run > 0.f) ? vsc / q_run : 0.f;
                         float *po = p.part_o + (slot * p.Hq + h) * p.d;
 #pragma unroll

@@ -213,9 +213,10 @@ def chunked(ctx_lens, q_lens, Hq, Hkv, d, seed, page_size=16, factor=1.0, causal
 @dataclass
 class PagedFP8:
     q: torch.Tensor           # [B, Hq, d] bf16
-    k_cache: torch.Tensor     # [P, page_size, Hkv, d] uint8 (FP8 E4M3 bytes)
+    k_cache: torch.Tensor     # [P, page_size, Hkv, d] uint8 (FP8 E4M3 bytes) or int8
     v_cache: torch.Tensor
-    k_scale: torch.Tensor     # [Hkv] float32: element c of head g stands for scale[g] * e4m3
+    k_scale: torch.Tensor     # [Hkv] float32: element c of head g stands for scale[g] *
+                              # e4m3 (or * int8)
     v_scale: torch.Tensor
     page_table: torch.Tensor  # int32 [B, maxp]
     seq_lens: torch.Tensor    # int32 [B]
@@ -232,11 +233,16 @@ def _to_e4m3(x: torch.Tensor):
     return q8.view(torch.uint8).contiguous(), sc
 
 
-def paged_fp8(lens, Hq, Hkv, d, seed, page_size=16, max_pages=None, factor=1.0,
-              scale=None) -> PagedFP8:
-    """The paged recipe above with the cache held as FP8 E4M3 bytes and one scale per
-    key/value head for K and for V: the same float32 draws, divided by the head's scale
-    and rounded to E4M3 (as a cache writer that quantises on append would)."""
+def _to_int8(x: torch.Tensor):
+    """float32 [P, ps, Hkv, d] -> (int8 values, per-head float32 scales) with each head's
+    largest magnitude mapped to 127 (symmetric: round to nearest even, -127 .. 127)."""
+    amax = x.abs().amax(dim=(0, 1, 3)).clamp_min(1e-30)
+    sc = (amax / 127.0).to(torch.float32)
+    q8 = torch.round(x / sc.view(1, 1, -1, 1)).clamp(-127.0, 127.0).to(torch.int8)
+    return q8.contiguous(), sc
+
+
+def _paged_bytes(lens, Hq, Hkv, d, seed, page_size, max_pages, factor, scale, quantise):
     lens = np.asarray(lens, np.int64)
     B = len(lens)
     npages = (lens + page_size - 1) // page_size
@@ -250,13 +256,30 @@ def paged_fp8(lens, Hq, Hkv, d, seed, page_size=16, max_pages=None, factor=1.0,
         table[b, :npages[b]] = perm[off:off + npages[b]]
         off += npages[b]
     q = normal_tensor((B, Hq, d), seed, TAG_Q, torch.bfloat16, factor)
-    kc, ks = _to_e4m3(normal_tensor((pool, page_size, Hkv, d), seed, TAG_K, torch.float32,
+    kc, ks = quantise(normal_tensor((pool, page_size, Hkv, d), seed, TAG_K, torch.float32,
                                     factor))
-    vc, vs = _to_e4m3(normal_tensor((pool, page_size, Hkv, d), seed, TAG_V, torch.float32,
+    vc, vs = quantise(normal_tensor((pool, page_size, Hkv, d), seed, TAG_V, torch.float32,
                                     factor))
-    return PagedFP8(q, kc, vc, ks, vs, torch.from_numpy(table),
-                    torch.from_numpy(lens.astype(np.int32)),
-                    (1.0 / math.sqrt(d)) if scale is None else scale)
+    return (q, kc, vc, ks, vs, torch.from_numpy(table), torch.from_numpy(lens.astype(np.int32)),
+            (1.0 / math.sqrt(d)) if scale is None else scale)
+
+
+def paged_fp8(lens, Hq, Hkv, d, seed, page_size=16, max_pages=None, factor=1.0,
+              scale=None) -> PagedFP8:
+    """The paged recipe above with the cache held as FP8 E4M3 bytes and one scale per
+    key/value head for K and for V: the same float32 draws, divided by the head's scale
+    and rounded to E4M3 (as a cache writer that quantises on append would)."""
+    return PagedFP8(*_paged_bytes(lens, Hq, Hkv, d, seed, page_size, max_pages, factor, scale,
+                                  _to_e4m3))
+
+
+def paged_int8(lens, Hq, Hkv, d, seed, page_size=16, max_pages=None, factor=1.0,
+               scale=None) -> PagedFP8:
+    """The same recipe with the cache held as INT8 (k_cache / v_cache torch.int8) and one
+    scale per key/value head for K and for V: the float32 draws divided by the head's
+    scale and rounded to the nearest integer in -127 .. 127."""
+    return PagedFP8(*_paged_bytes(lens, Hq, Hkv, d, seed, page_size, max_pages, factor, scale,
+                                  _to_int8))
 
 
 @dataclass
@@ -308,6 +331,13 @@ WORKLOADS = {
         dict(B=64, lo=1024, hi=32768, Hq=32, Hkv=8, d=128, page_size=16, factor=1.0),
         "B=64 one query each, lengths U[1024,32768], Hq=32 Hkv=8 d=128, 16-token pages, "
         "permuted page table, N(0,1) cache quantised to FP8 E4M3 with per-head scales"),
+    # the decode workload with the cache quantised to INT8 (one scale per key/value
+    # head), the other format the KV-cache glossary entry names
+    "decode_paged_int8_b64": Workload(
+        "decode_paged_int8_b64", "decode_int8", 5,
+        dict(B=64, lo=1024, hi=32768, Hq=32, Hkv=8, d=128, page_size=16, factor=1.0),
+        "B=64 one query each, lengths U[1024,32768], Hq=32 Hkv=8 d=128, 16-token pages, "
+        "permuted page table, N(0,1) cache quantised to INT8 with per-head scales"),
     # chunked prefill with prefix caching: 8 sequences whose cached prefixes are
     # U[1024, 16384] tokens each receive a chunk of 2048 new tokens, which attend
     # causally to the prefix and to themselves through the page table
@@ -360,10 +390,10 @@ def make(name: str, batch: int | None = None):
         ql = np.full(B, p["chunk"], np.int64)
         return chunked(prefix + ql, ql, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"],
                        p["factor"])
-    if w.kind == "decode_fp8":
+    if w.kind in ("decode_fp8", "decode_int8"):
         B = p["B"] if batch is None else int(batch)
         lens = lengths(B, p["lo"], p["hi"], w.seed)
         maxp = (p["hi"] + p["page_size"] - 1) // p["page_size"]
-        return paged_fp8(lens, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"], maxp,
-                         p["factor"])
+        gen = paged_fp8 if w.kind == "decode_fp8" else paged_int8
+        return gen(lens, p["Hq"], p["Hkv"], p["d"], w.seed, p["page_size"], maxp, p["factor"])
     raise ValueError(w.kind)

@@ -167,8 +167,9 @@ KERNEL_SOURCES = {
     "prefill_simt_kernel": ("prefill_simt.cuh", "ptx.cuh"),
     "prefill_simt_rows_kernel<4>": ("prefill_simt.cuh", "ptx.cuh"),
     "prefill_simt_rows_kernel<2>": ("prefill_simt.cuh", "ptx.cuh"),
-    "decode_split_kernel": ("decode.cuh", "ptx.cuh"),
-    "decode_split_kernel<true>": ("decode.cuh", "ptx.cuh"),
+    "decode_split_kernel<0>": ("decode.cuh", "ptx.cuh"),
+    "decode_split_kernel<1>": ("decode.cuh", "ptx.cuh"),
+    "decode_split_kernel<2>": ("decode.cuh", "ptx.cuh"),
 }
 
 
@@ -257,7 +258,7 @@ def nbytes(*ts) -> int:
 
 def workload_shape(kind, w, spec):
     """The workload's sizes as the JSON line's config reports them (both arms)."""
-    if kind in ("decode", "decode_fp8"):
+    if kind in ("decode", "decode_fp8", "decode_int8"):
         B, Hq, d = w.q.shape
         shape = {"B": B, "Hq": Hq, "Hkv": int(w.k_cache.shape[2]), "d": d,
                  "page_size": int(w.k_cache.shape[1]), "total_tokens": int(w.seq_lens.sum())}
@@ -301,9 +302,9 @@ class Leg:
         w = inputs.make(name, batch)
         self.w = w
         self.scale = w.scale
-        if self.kind in ("decode", "decode_fp8"):
+        if self.kind in ("decode", "decode_fp8", "decode_int8"):
             self.host = [w.q, w.k_cache, w.v_cache, w.page_table, w.seq_lens]
-            if self.kind == "decode_fp8":
+            if self.kind in ("decode_fp8", "decode_int8"):
                 self.host += [w.k_scale, w.v_scale]
             self.dev = [t.to(dev) for t in self.host]
             q, kc = self.dev[0], self.dev[1]
@@ -314,7 +315,9 @@ class Leg:
                                                                kc.shape[1]),
                                   dtype=torch.uint8, device=dev)
             self.work, self.unit, self.bound = decode_bytes(w), "GB/s", "hbm"
-            self.kernel = "decode_split_kernel" + ("<true>" if self.kind == "decode_fp8" else "")
+            # (the split kernel's template argument: 0 bf16, 1 FP8, 2 INT8 cache)
+            self.kernel = "decode_split_kernel<%d>" % {"decode": 0, "decode_fp8": 1,
+                                                       "decode_int8": 2}[self.kind]
         else:
             if self.kind == "chunk":
                 self.host = [w.q, w.k_cache, w.v_cache, w.page_table, w.seq_lens, w.cu_seqlens_q]
@@ -343,10 +346,10 @@ class Leg:
         # its O and LSE go back, while the cache stays resident on the device (where a
         # serving process keeps it between steps); every other workload copies all of
         # its inputs in
-        self.e2e_in = ([0, 3, 4] if self.kind in ("decode", "decode_fp8")
+        self.e2e_in = ([0, 3, 4] if self.kind in ("decode", "decode_fp8", "decode_int8")
                        else list(range(len(self.host))))
         self.resident = (nbytes(*[t for i, t in enumerate(self.host) if i not in self.e2e_in])
-                         if self.kind in ("decode", "decode_fp8") else 0)
+                         if self.kind in ("decode", "decode_fp8", "decode_int8") else 0)
         self.h2d = nbytes(*[self.host[i] for i in self.e2e_in])
         self.d2h = nbytes(self.o, self.lse)
 
@@ -358,6 +361,9 @@ class Leg:
         elif self.kind == "decode_fp8":
             A.attn_decode_paged_fp8(d[0], d[1], d[2], d[5], d[6], d[3], d[4], self.scale,
                                     o=self.o, lse=self.lse, workspace=self.ws, stream=stream)
+        elif self.kind == "decode_int8":
+            A.attn_decode_paged_int8(d[0], d[1], d[2], d[5], d[6], d[3], d[4], self.scale,
+                                     o=self.o, lse=self.lse, workspace=self.ws, stream=stream)
         elif self.kind == "chunk":
             A.attn_fwd_chunked_paged(d[0], d[1], d[2], d[3], d[4], d[5], self.max_len,
                                      self.w.causal, self.scale, o=self.o, lse=self.lse,
@@ -421,7 +427,7 @@ def simt_kernel(q_shape, dev) -> str:
 
 
 def launches_per_call(leg) -> int:
-    return 2 if leg.kind in ("decode", "decode_fp8", "two_pass") else 1
+    return 2 if leg.kind in ("decode", "decode_fp8", "decode_int8", "two_pass") else 1
 
 
 _ORACLE_INPUTS = {}
@@ -468,16 +474,17 @@ def cpu_oracle_sample(w, kind: str, seconds: float, seed: int = 0):
             if el >= seconds:
                 return work / el / 1e12, el, "%d random query rows (%.1f s, fp64)" % (done, el), \
                     oracle.max_threads()
-    if kind == "decode_fp8":
-        args = _oracle_inputs(w, "decode_fp8", lambda: (
+    if kind in ("decode_fp8", "decode_int8"):
+        args = _oracle_inputs(w, kind, lambda: (
             w.q.float().numpy(), w.k_cache.numpy(), w.v_cache.numpy(), w.k_scale.numpy(),
             w.v_scale.numpy(), w.page_table.numpy(), w.seq_lens.numpy()))
+        fn = oracle.decode_paged_fp8 if kind == "decode_fp8" else oracle.decode_paged_int8
         sl = w.seq_lens.numpy()
         Hkv, d = w.k_cache.shape[2], w.k_cache.shape[3]
         t0 = time.perf_counter()
         while True:
             b = int(rng.integers(0, len(sl)))
-            oracle.decode_paged_fp8(*args, w.scale, seqs=[b])
+            fn(*args, w.scale, seqs=[b])
             work += 2.0 * Hkv * d * 1.0 * float(sl[b])
             done += 1
             el = time.perf_counter() - t0
@@ -727,7 +734,8 @@ def run_gpu(args):
             "ms_per_step": sum(leg_ms) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("f32" if getattr(p0, "f32", False) else
-                      "f16 (E4M3 cache)" if p0.kind == "decode_fp8" else "bf16"),
+                      "f16 (E4M3 cache)" if p0.kind == "decode_fp8" else
+                      "f16 (INT8 cache)" if p0.kind == "decode_int8" else "bf16"),
             "data": "synthetic",
             "config": config,
             "roofline": roofs[0],

@@ -295,6 +295,32 @@ attn_status_t attn_decode_paged_fp8(const void *q, const void *k_cache, const vo
                                     attn_stream_t stream);
 
 /*
+ * attn_decode_paged_int8 -- attn_decode_paged against a cache held as 8-bit
+ * integers (the same "KV Cache" entry of the yapayzekasozluk.tr "attention" tag
+ * page: INT8 or FP8 storage of the cache, 2-4x less memory).  The decode reads
+ * half the bytes of a bf16 cache, like the FP8 form.
+ *   k_cache,
+ *   v_cache     [num_pages, page_size, Hkv, d] int8 (two's complement bytes,
+ *               -128 .. 127)
+ *   k_scale,
+ *   v_scale     float32 [Hkv], DEVICE pointers: element c of head g of a cached key
+ *               (value) stands for k_scale[g] * int8 (v_scale[g] * int8)
+ *   q, o, lse, page_table, seq_lens, workspace and their rules as attn_decode_paged.
+ *   Inside the kernel the cache is widened to f16 (exactly: every int8 is an f16)
+ *   and q is rounded to f16 (exact for |q| below 65504; larger values are not
+ *   supported); scores and sums are fp32.  Null k_scale or v_scale returns
+ *   ATTN_ERR_INVALID_ARG.  Supported: d == 128, page_size == 16, Hkv <= 8,
+ *   Hq/Hkv <= 8.
+ */
+attn_status_t attn_decode_paged_int8(const void *q, const void *k_cache, const void *v_cache,
+                                     const float *k_scale, const float *v_scale,
+                                     const int32_t *page_table, const int32_t *seq_lens, void *o,
+                                     float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                                     int num_pages, int max_pages_per_seq, float scale,
+                                     void *workspace, size_t workspace_bytes,
+                                     attn_stream_t stream);
+
+/*
  * attn_decode_paged_window -- attn_decode_paged where the new query attends only
  * to the last window + 1 cached tokens of its sequence (positions
  * seq_lens[b] - 1 - window .. seq_lens[b] - 1): the decode side of local

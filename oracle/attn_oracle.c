@@ -515,20 +515,22 @@ double oracle_e4m3_value(uint8_t x)
 }
 
 /*
- * Decode against a paged cache held as FP8 E4M3 bytes (yapayzekasozluk.tr
+ * Decode against a paged cache held as one byte per element (yapayzekasozluk.tr
  * "attention" tag page, entry "KV Cache": the cache may be kept in INT8/FP8 to
  * cut its memory 2-4x).  Cached key (value) element c of head g stands for
- * k_scale[g] * e4m3(byte) (v_scale[g] * e4m3(byte)); the query attends to
- * those dequantised values exactly as in oracle_decode_paged_rows.  The bytes
- * are dequantised here in fp64, row by row, into scratch rows.
+ * k_scale[g] * value(byte) (v_scale[g] * value(byte)), value() being the byte
+ * format's rule; the query attends to those dequantised values exactly as in
+ * oracle_decode_paged_rows.  The bytes are dequantised here in fp64, row by
+ * row, into scratch rows.
  */
-int oracle_decode_paged_fp8_rows(const float *q, const uint8_t *k_cache, const uint8_t *v_cache,
-                                 const float *k_scale, const float *v_scale,
-                                 const int32_t *page_table, const int32_t *seq_lens,
-                                 int B, int Hq, int Hkv, int d, int page_size,
-                                 int num_pages, int maxp, double scale,
-                                 const int32_t *seqs, int nseq,
-                                 double *o_rows, double *lse_rows, int nthreads)
+static int decode_paged_bytes_rows(double (*value)(uint8_t), const float *q,
+                                   const uint8_t *k_cache, const uint8_t *v_cache,
+                                   const float *k_scale, const float *v_scale,
+                                   const int32_t *page_table, const int32_t *seq_lens,
+                                   int B, int Hq, int Hkv, int d, int page_size,
+                                   int num_pages, int maxp, double scale,
+                                   const int32_t *seqs, int nseq,
+                                   double *o_rows, double *lse_rows, int nthreads)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || page_size <= 0)
         return -1;
@@ -550,7 +552,7 @@ int oracle_decode_paged_fp8_rows(const float *q, const uint8_t *k_cache, const u
 #pragma omp parallel num_threads(nt)
     {
         double *s = (double *)malloc(sizeof(double) * (size_t)cap);
-        /* dequantised key/value rows in fp64 (k_scale * e4m3 is not always a float,
+        /* dequantised key/value rows in fp64 (scale * value is not always a float,
          * so the definition is written out again below on double rows instead of
          * going through attention_row, which reads float rows) */
         double *kd = (double *)malloc(sizeof(double) * (size_t)cap * d);
@@ -572,8 +574,8 @@ int oracle_decode_paged_fp8_rows(const float *q, const uint8_t *k_cache, const u
                 const int64_t page = page_table[(int64_t)b * maxp + t / page_size];
                 const int64_t off = ((page * page_size + t % page_size) * Hkv + g) * d;
                 for (int c = 0; c < d; ++c) {
-                    kd[t * d + c] = (double)k_scale[g] * oracle_e4m3_value(k_cache[off + c]);
-                    vd[t * d + c] = (double)v_scale[g] * oracle_e4m3_value(v_cache[off + c]);
+                    kd[t * d + c] = (double)k_scale[g] * value(k_cache[off + c]);
+                    vd[t * d + c] = (double)v_scale[g] * value(v_cache[off + c]);
                 }
             }
             /* the definition, as in attention_row, on the dequantised rows */
@@ -603,6 +605,41 @@ int oracle_decode_paged_fp8_rows(const float *q, const uint8_t *k_cache, const u
         free(vd);
     }
     return 0;
+}
+
+/* The FP8 E4M3 cache: value(byte) = e4m3(byte) (oracle_e4m3_value above). */
+int oracle_decode_paged_fp8_rows(const float *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *page_table, const int32_t *seq_lens,
+                                 int B, int Hq, int Hkv, int d, int page_size,
+                                 int num_pages, int maxp, double scale,
+                                 const int32_t *seqs, int nseq,
+                                 double *o_rows, double *lse_rows, int nthreads)
+{
+    return decode_paged_bytes_rows(oracle_e4m3_value, q, k_cache, v_cache, k_scale, v_scale,
+                                   page_table, seq_lens, B, Hq, Hkv, d, page_size, num_pages,
+                                   maxp, scale, seqs, nseq, o_rows, lse_rows, nthreads);
+}
+
+/* The value of one INT8 byte: the byte read as a two's complement integer,
+ * -128 .. 127. */
+double oracle_int8_value(uint8_t x)
+{
+    return x < 128 ? (double)x : (double)x - 256.0;
+}
+
+/* The INT8 cache: value(byte) = int8(byte). */
+int oracle_decode_paged_int8_rows(const float *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                  const float *k_scale, const float *v_scale,
+                                  const int32_t *page_table, const int32_t *seq_lens,
+                                  int B, int Hq, int Hkv, int d, int page_size,
+                                  int num_pages, int maxp, double scale,
+                                  const int32_t *seqs, int nseq,
+                                  double *o_rows, double *lse_rows, int nthreads)
+{
+    return decode_paged_bytes_rows(oracle_int8_value, q, k_cache, v_cache, k_scale, v_scale,
+                                   page_table, seq_lens, B, Hq, Hkv, d, page_size, num_pages,
+                                   maxp, scale, seqs, nseq, o_rows, lse_rows, nthreads);
 }
 
 /*

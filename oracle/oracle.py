@@ -60,6 +60,10 @@ def _load():
         lib.oracle_e4m3_value.restype = D
         lib.oracle_decode_paged_fp8_rows.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, D,
                                                      P, I, P, P, I]
+        lib.oracle_int8_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_int8_value.restype = D
+        lib.oracle_decode_paged_int8_rows.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I,
+                                                      D, P, I, P, P, I]
         lib.oracle_chunk_paged_rows.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I,
                                                 D, P, I64, P, P, I]
         lib.oracle_online_softmax_stats.argtypes = [P, I64, I64, P, P]
@@ -69,7 +73,8 @@ def _load():
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_attn_rows", "oracle_attn_fwd", "oracle_attn_varlen",
                      "oracle_attn_window_rows", "oracle_decode_paged_window_rows",
-                     "oracle_decode_paged_fp8_rows", "oracle_chunk_paged_rows",
+                     "oracle_decode_paged_fp8_rows", "oracle_decode_paged_int8_rows",
+                     "oracle_chunk_paged_rows",
                      "oracle_decode_paged_rows", "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -256,14 +261,18 @@ def e4m3_value(byte: int) -> float:
     return float(_load().oracle_e4m3_value(int(byte) & 0xFF))
 
 
-def decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
-                     scale: float, seqs=None, nthreads: int = 0):
-    """Decode against an FP8 E4M3 paged cache: k_cache/v_cache uint8 [P,page_size,Hkv,d]
-    (E4M3 bytes), k_scale/v_scale [Hkv] (element c of head g stands for scale[g] *
-    e4m3(byte)).  Other arguments and results as decode_paged."""
+def _bytes(x):
+    """A one-byte cache as uint8: int8 arrays keep their bytes, others are cast."""
+    a = np.asarray(x)
+    if a.dtype == np.int8:
+        return np.ascontiguousarray(a).view(np.uint8)
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def _decode_paged_bytes(fn, name, q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                        scale, seqs, nthreads):
     q = _f32(q)
-    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
-    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    kc, vc = _bytes(k_cache), _bytes(v_cache)
     ks, vs = _f32(k_scale), _f32(v_scale)
     pt, sl = _i32(page_table), _i32(seq_lens)
     B, Hq, d = q.shape
@@ -274,12 +283,36 @@ def decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens
     n = seqs.shape[0]
     o = np.zeros((n, Hq, d), np.float64)
     lse = np.zeros((n, Hq), np.float64)
-    rc = _load().oracle_decode_paged_fp8_rows(_p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(pt),
-                                              _p(sl), B, Hq, Hkv, d, ps, P, maxp, float(scale),
-                                              _p(seqs), n, _p(o), _p(lse), int(nthreads))
+    rc = fn(_p(q), _p(kc), _p(vc), _p(ks), _p(vs), _p(pt), _p(sl), B, Hq, Hkv, d, ps, P, maxp,
+            float(scale), _p(seqs), n, _p(o), _p(lse), int(nthreads))
     if rc != 0:
-        raise ValueError("oracle_decode_paged_fp8_rows rejected its arguments")
+        raise ValueError(name + " rejected its arguments")
     return o, lse
+
+
+def decode_paged_fp8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                     scale: float, seqs=None, nthreads: int = 0):
+    """Decode against an FP8 E4M3 paged cache: k_cache/v_cache uint8 [P,page_size,Hkv,d]
+    (E4M3 bytes), k_scale/v_scale [Hkv] (element c of head g stands for scale[g] *
+    e4m3(byte)).  Other arguments and results as decode_paged."""
+    return _decode_paged_bytes(_load().oracle_decode_paged_fp8_rows,
+                               "oracle_decode_paged_fp8_rows", q, k_cache, v_cache, k_scale,
+                               v_scale, page_table, seq_lens, scale, seqs, nthreads)
+
+
+def int8_value(byte: int) -> float:
+    """The value of one INT8 byte (two's complement)."""
+    return float(_load().oracle_int8_value(int(byte) & 0xFF))
+
+
+def decode_paged_int8(q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens,
+                      scale: float, seqs=None, nthreads: int = 0):
+    """Decode against an INT8 paged cache: k_cache/v_cache int8 (or their bytes as uint8)
+    [P,page_size,Hkv,d], k_scale/v_scale [Hkv] (element c of head g stands for scale[g] *
+    int8).  Other arguments and results as decode_paged."""
+    return _decode_paged_bytes(_load().oracle_decode_paged_int8_rows,
+                               "oracle_decode_paged_int8_rows", q, k_cache, v_cache, k_scale,
+                               v_scale, page_table, seq_lens, scale, seqs, nthreads)
 
 
 def online_softmax_stats(x, block: int):

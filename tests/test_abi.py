@@ -105,6 +105,30 @@ def test_varlen_and_decode_validation(lib):
                                    None) == A.ATTN_ERR_INVALID_ARG
 
 
+def test_byte_cache_decode_validation(lib):
+    """The FP8 and INT8 decodes need both per-head scale arrays and take d = 128 only;
+    their other rules are attn_decode_paged's."""
+    P = ctypes.c_void_p
+    p = P(1 << 20)
+    # q, k_cache, v_cache, k_scale, v_scale, page_table, seq_lens, o, lse, B, Hq, Hkv, d,
+    # page_size, num_pages, max_pages_per_seq, scale, workspace, bytes, stream
+    for fn in (lib.attn_decode_paged_fp8, lib.attn_decode_paged_int8):
+        ok = [p, p, p, p, p, p, p, p, None, 4, 32, 8, 128, 16, 100, 10, 0.1, p, 1 << 30, None]
+        for i in (3, 4):                       # a missing scale array
+            bad = list(ok)
+            bad[i] = None
+            assert fn(*bad) == A.ATTN_ERR_INVALID_ARG, (fn, i)
+        d64 = list(ok)
+        d64[12] = 64
+        assert fn(*d64) == A.ATTN_ERR_UNSUPPORTED
+        ps32 = list(ok)
+        ps32[13] = 32
+        assert fn(*ps32) == A.ATTN_ERR_UNSUPPORTED
+        no_ws = list(ok)
+        no_ws[17] = None
+        assert fn(*no_ws) == A.ATTN_ERR_INVALID_ARG
+
+
 def test_f32_head_dim_rule(lib):
     """attn_fwd_f32 implements 16 <= d <= 128 with d % 16 == 0, as its header states."""
     P = ctypes.c_void_p
