@@ -71,3 +71,17 @@ def test_decode_bytes_per_token():
     assert bench.decode_bytes(p) == 2.0 * 4 * 128 * 2 * sum(lens)
     f = inputs.paged_fp8(lens, 8, 4, 128, 5)
     assert bench.decode_bytes(f) == 2.0 * 4 * 128 * 1 * sum(lens)
+    i8 = inputs.paged_int8(lens, 8, 4, 128, 5)
+    assert bench.decode_bytes(i8) == 2.0 * 4 * 128 * 1 * sum(lens)
+
+
+def test_every_workload_has_a_config_and_a_kernel_name():
+    """Each named workload maps to a config key and, on the device, to a kernel whose
+    sources the fingerprint covers (no workload is left without its traffic lookup)."""
+    kinds = {w.kind for w in inputs.WORKLOADS.values()}
+    assert {"dense", "varlen", "decode", "decode_fp8", "decode_int8", "chunk", "window",
+            "two_pass"} <= kinds
+    for k in ("decode_split_kernel<0>", "decode_split_kernel<1>", "decode_split_kernel<2>",
+              "prefill_tc_kernel", "prefill_simt_kernel", "prefill_simt_rows_kernel<4>",
+              "prefill_simt_rows_kernel<2>"):
+        assert len(bench.kernel_fingerprint(k)) == 16
