@@ -4,8 +4,7 @@ the reference arm's non-zero ranks do no work."""
 import os
 import socket
 
-import pytest
-import torch
+port torch
 import torch.multiprocessing as mp
 
 import bench
@@ -101,19 +100,28 @@ def test_kernel_fingerprint_ignores_comments_only():
     assert bench.kernel_fingerprint("prefill_tc_kernel", reader(edited)) != fp
 
 
-def test_reference_arm_prints_one_contract_line():
+import pytest
+
+
+@pytest.mark.parametrize("name,batch,cfg_key,unit", [
+    ("single_head_f32", None, "prefill", "TFLOP/s"),
+    ("decode_paged_int8_b64", 2, "decode_int8", "GB/s"),
+])
+def test_reference_arm_prints_one_contract_line(name, batch, cfg_key, unit):
     """`bench.py --impl reference` (the fp64 oracle on the host cores) prints one JSON line
-    with the keys and types the benchmark contract names, on the same metric as our arm."""
+    with the keys and types the benchmark contract names, on the same metric as our arm
+    (a prefill workload, and a decode one with its batch cut to 2 sequences)."""
     import json
     import os
     import subprocess
     import sys
 
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
-                          "--workload", "single_head_f32", "--steps", "3", "--warmup", "3",
-                          "--ref-seconds", "1"], capture_output=True, text=True, timeout=300,
-                         cwd=root)
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+           "--workload", name, "--steps", "3", "--warmup", "3", "--ref-seconds", "1"]
+    if batch is not None:
+        cmd += ["--batch", str(batch)]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=root)
     assert out.returncode == 0, out.stderr[-2000:]
     lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1, out.stdout
@@ -129,8 +137,9 @@ def test_reference_arm_prints_one_contract_line():
     assert d["vs_baseline"] is None
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["unit"] == unit
     # the config names the workload's sizes exactly as the GPU arm's line does
     from attn_fwd_07_b300 import inputs
-    spec = inputs.WORKLOADS["single_head_f32"]
-    assert d["config"]["prefill"] == bench.workload_shape(spec.kind, inputs.make(spec.name),
-                                                          spec)
+    spec = inputs.WORKLOADS[name]
+    assert d["config"][cfg_key] == bench.workload_shape(spec.kind,
+                                                        inputs.make(spec.name, batch), spec)
