@@ -4,7 +4,8 @@ the reference arm's non-zero ranks do no work."""
 import os
 import socket
 
-port torch
+import pytest
+import torch
 import torch.multiprocessing as mp
 
 import bench
@@ -98,9 +99,6 @@ def test_kernel_fingerprint_ignores_comments_only():
     assert bench.kernel_fingerprint("prefill_tc_kernel", reader(commented)) == fp
     edited = dict(base, **{"prefill_tc.cuh": b"int f() {\n  return 2;\n}\n"})
     assert bench.kernel_fingerprint("prefill_tc_kernel", reader(edited)) != fp
-
-
-import pytest
 
 
 @pytest.mark.parametrize("name,batch,cfg_key,unit", [
